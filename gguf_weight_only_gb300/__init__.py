@@ -1,0 +1,132 @@
+"""GB300 (sm_103a) GGUF weight-only quantized linear layer: Python binding.
+
+Thin ctypes marshalling over the C ABI in include/qlinear.h (library
+gguf_weight_only_gb300/_lib/libqlinear.so, built by `gguf_weight_only_gb300.build`). Every
+step of the computation runs in the library's CUDA kernels; PyTorch only provides device
+memory and the current stream. There is no CPU fallback: if the library is missing, every
+call raises.
+
+    y = qlinear(W_u8_cuda, ggml_type, N, K, x_f16_cuda)      # -> (M, N) float32 cuda
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libqlinear.so")
+
+Q4_K, Q5_K, Q6_K, IQ4_XS = 12, 13, 14, 23
+STATUS = {0: "QL_OK", -1: "QL_ERR_TYPE", -2: "QL_ERR_SHAPE", -3: "QL_ERR_NULL", -4: "QL_ERR_ALIGN",
+          -5: "QL_ERR_CUDA", -6: "QL_ERR_TIMEOUT", -7: "QL_ERR_UNSUPPORTED", -8: "QL_ERR_DEVICE"}
+# Every function include/qlinear.h declares (the symbol-export test checks this list
+# against the header).
+EXPORTS = ("qlinear", "qlinear_gemv", "qlinear_gemm", "qlinear_block_bytes", "qlinear_gemv_max_m",
+           "qlinear_strerror", "qlinear_last_cuda_error", "qlinear_device_status", "qlinear_launch_count")
+
+_lib = None
+
+
+class QLinearError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"CUDA library not built: {LIB_PATH} (run gguf_weight_only_gb300.build.build())")
+        l = ctypes.CDLL(LIB_PATH)
+        i64, vp = ctypes.c_int64, ctypes.c_void_p
+        for name in ("qlinear", "qlinear_gemv", "qlinear_gemm"):
+            f = getattr(l, name)
+            f.argtypes = [ctypes.c_int, vp, i64, i64, vp, i64, vp, vp]
+            f.restype = ctypes.c_int
+        l.qlinear_block_bytes.argtypes = [ctypes.c_int]
+        l.qlinear_block_bytes.restype = ctypes.c_int
+        l.qlinear_gemv_max_m.argtypes = []
+        l.qlinear_gemv_max_m.restype = ctypes.c_int
+        l.qlinear_strerror.argtypes = [ctypes.c_int]
+        l.qlinear_strerror.restype = ctypes.c_char_p
+        l.qlinear_last_cuda_error.argtypes = []
+        l.qlinear_last_cuda_error.restype = ctypes.c_int
+        l.qlinear_device_status.argtypes = [vp]
+        l.qlinear_device_status.restype = ctypes.c_int
+        l.qlinear_launch_count.argtypes = [ctypes.c_int, i64, i64, i64]
+        l.qlinear_launch_count.restype = ctypes.c_int
+        _lib = l
+    return _lib
+
+
+def strerror(status: int) -> str:
+    return lib().qlinear_strerror(int(status)).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        extra = ""
+        if status == -5:
+            extra = f" (cudaError {lib().qlinear_last_cuda_error()})"
+        raise QLinearError(status, f"{what}: {STATUS.get(status, status)}: {strerror(status)}{extra}")
+
+
+def block_bytes(ggml_type: int) -> int:
+    return lib().qlinear_block_bytes(int(ggml_type))
+
+
+def gemv_max_m() -> int:
+    return lib().qlinear_gemv_max_m()
+
+
+def launch_count(ggml_type: int, N: int, K: int, M: int) -> int:
+    return lib().qlinear_launch_count(int(ggml_type), int(N), int(K), int(M))
+
+
+def _stream_handle(stream) -> int:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def qlinear_raw(path: str, ggml_type: int, W_ptr: int, N: int, K: int, x_ptr: int, M: int, y_ptr: int,
+                stream_handle: int) -> None:
+    """Direct C-ABI call on raw device pointers (no checks beyond the library's own)."""
+    fn = {"auto": lib().qlinear, "gemv": lib().qlinear_gemv, "gemm": lib().qlinear_gemm}[path]
+    _check(fn(int(ggml_type), W_ptr, int(N), int(K), x_ptr, int(M), y_ptr, stream_handle), f"qlinear[{path}]")
+
+
+def qlinear(W, ggml_type: int, N: int, K: int, x, out=None, path: str = "auto", stream=None):
+    """y[M, N] float32 = x[M, K] (fp16) . dequant(W)^T on the current CUDA stream.
+
+    W: uint8 CUDA tensor holding N*K/256 packed superblocks (contiguous, 16-byte aligned).
+    x: float16 CUDA tensor of shape (M, K) or (K,). path: "auto" | "gemv" | "gemm".
+    """
+    import torch
+    if not (isinstance(W, torch.Tensor) and W.is_cuda and W.dtype == torch.uint8):
+        raise TypeError("W must be a uint8 CUDA tensor")
+    if not (isinstance(x, torch.Tensor) and x.is_cuda and x.dtype == torch.float16):
+        raise TypeError("x must be a float16 CUDA tensor")
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    if x.dim() != 2 or x.shape[1] != K:
+        raise ValueError(f"x must have shape (M, {K})")
+    if not (W.is_contiguous() and x.is_contiguous()):
+        raise ValueError("W and x must be contiguous")
+    bb = block_bytes(ggml_type)
+    if bb > 0 and W.numel() < N * (K // 256) * bb:
+        raise ValueError("W holds fewer bytes than N*K/256 superblocks")
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    elif not (out.is_cuda and out.dtype == torch.float32 and out.is_contiguous() and out.numel() >= M * N):
+        raise ValueError("out must be a contiguous float32 CUDA tensor with M*N elements")
+    qlinear_raw(path, ggml_type, W.data_ptr(), N, K, x.data_ptr(), M, out.data_ptr(), _stream_handle(stream))
+    return out
+
+
+def device_status(stream=None) -> int:
+    """Synchronise and return the device status word (0, or QL_ERR_TIMEOUT / QL_ERR_CUDA)."""
+    return lib().qlinear_device_status(_stream_handle(stream))

@@ -1,0 +1,117 @@
+/*
+ * qlinear.h -- C ABI of the GB300 (sm_103a) GGUF weight-only quantized linear layer.
+ *
+ * The layer computes, for a weight matrix W stored as GGUF/ggml superblocks of 256 weights,
+ *
+ *     y[m][n] = sum_{k<K} x[m][k] * dequant(W)[n][k]          m < M, n < N
+ *
+ * with fp16 activations x, fp32 accumulation and an fp32 result y. Supported block formats
+ * (ggml type id: bytes per 256-weight superblock), from the _GGML_QUANT table of
+ * tinygrad/llm/gguf.py:
+ *     Q4_K   = 12 : 144     d, dmin fp16; 12-byte packed 6-bit scales/mins; 128 B of 4-bit q
+ *     Q5_K   = 13 : 176     as Q4_K plus a 32-byte high-bit array (commit log of explicit-dev,
+ *                           commit "custom kernels: Q4_K support (ggml type 12)")
+ *     Q6_K   = 14 : 210     128 B low 4 bits, 64 B high 2 bits, 16 int8 scales, d fp16 last
+ *     IQ4_XS = 23 : 136     d fp16; 6-bit per-32 scales; 4-bit indices into a 16-entry
+ *                           non-linear codebook (test/unit/test_llm_quant_cpu.py,
+ *                           test_unpack_lut_dot_uop)
+ * Dequantised weight: K-quants d*sc*q - dmin*m; Q6_K d*sc*(q-32); IQ4_XS d*(ls-32)*kv[q].
+ *
+ * Layouts (all row-major, contiguous, little-endian):
+ *   W_blocks : N rows x (K/256) superblocks; row n, superblock b at byte (n*K/256 + b)*BB.
+ *              This is the packed slice a GGUF file stores for an (N, K) tensor (dims
+ *              reversed, K fastest: tinygrad/llm/gguf.py, _gguf_parse).
+ *   x_fp16   : M x K IEEE binary16.
+ *   y_fp32   : M x N fp32, overwritten (never accumulated into).
+ *
+ * Ownership and execution: every pointer is a device pointer owned by the caller, on the
+ * current CUDA device. W and x are read-only. The call is asynchronous on `stream`
+ * (a cudaStream_t; NULL = the legacy default stream): it validates, enqueues and returns
+ * without synchronising. The library keeps a small per-device state (tensor-map cache,
+ * kernel attributes) created on first use and never frees caller memory. Calls on
+ * distinct streams may run concurrently; no scratch memory is shared between calls.
+ *
+ * Errors: arguments are checked on the host before any launch, and a failing check
+ * returns a negative ql_status with nothing enqueued. A failed launch returns
+ * QL_ERR_CUDA (qlinear_last_cuda_error() gives the cudaError_t, per calling thread).
+ * Device-side pipeline waits are bounded; a wait that runs out sets a device status
+ * word that qlinear_device_status() reports as QL_ERR_TIMEOUT.
+ */
+#ifndef QLINEAR_H_
+#define QLINEAR_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QL_Q4_K = 12,
+    QL_Q5_K = 13,
+    QL_Q6_K = 14,
+    QL_IQ4_XS = 23
+} ql_type;
+
+typedef enum {
+    QL_OK = 0,
+    QL_ERR_TYPE = -1,        /* unsupported ggml type */
+    QL_ERR_SHAPE = -2,       /* K % 256 != 0, N < 1, M < 1, or a size beyond int32 indexing */
+    QL_ERR_NULL = -3,        /* a required pointer is NULL */
+    QL_ERR_ALIGN = -4,       /* W, x or y not 16-byte aligned */
+    QL_ERR_CUDA = -5,        /* a CUDA runtime call or kernel launch failed */
+    QL_ERR_TIMEOUT = -6,     /* a device-side bounded wait ran out (see qlinear_device_status) */
+    QL_ERR_UNSUPPORTED = -7, /* the forced path cannot run this shape on this device */
+    QL_ERR_DEVICE = -8       /* the current device is not an sm_103 (GB300) part */
+} ql_status;
+
+/*
+ * qlinear: y = x . dequant(W)^T, dispatched on M.
+ *   M <= qlinear_gemv_max_m()  -> decode kernel (tensor-core mma.sync GEMV, weights
+ *                                 streamed once from HBM through a TMA-fed shared ring)
+ *   otherwise                   -> prefill kernel (tcgen05 MMA with TMEM accumulators)
+ * Chunked prefill pads M to the MMA tile internally; padded rows are never stored
+ * (commit log of explicit-dev: "quant linears pad to the chunk bucket").
+ * Arguments: type = ql_type; W_blocks = packed weights (N*K/256*BB bytes, 16-byte aligned);
+ * N, K = output / input features (K % 256 == 0); x_fp16 = activations (M*K halves,
+ * 16-byte aligned); M = tokens; y_fp32 = output (M*N floats, 16-byte aligned);
+ * stream = cudaStream_t or NULL. Returns QL_OK or a negative ql_status.
+ */
+int qlinear(int type, const void *W_blocks, int64_t N, int64_t K, const void *x_fp16, int64_t M,
+            float *y_fp32, void *stream);
+
+/* Same contract, forcing the decode (GEMV) kernel for any M >= 1. Tokens are processed in
+ * groups of 8 per MMA; the packed weights are decoded once per call. */
+int qlinear_gemv(int type, const void *W_blocks, int64_t N, int64_t K, const void *x_fp16, int64_t M,
+                 float *y_fp32, void *stream);
+
+/* Same contract, forcing the prefill (tcgen05) kernel for any M >= 1. */
+int qlinear_gemm(int type, const void *W_blocks, int64_t N, int64_t K, const void *x_fp16, int64_t M,
+                 float *y_fp32, void *stream);
+
+/* Bytes per 256-weight superblock of `type` (144/176/210/136), or QL_ERR_TYPE. */
+int qlinear_block_bytes(int type);
+
+/* Largest M that qlinear() sends to the decode kernel (8). */
+int qlinear_gemv_max_m(void);
+
+/* Static description of a status code; never NULL. */
+const char *qlinear_strerror(int status);
+
+/* cudaError_t recorded by the last QL_ERR_CUDA returned on the calling thread (0 if none). */
+int qlinear_last_cuda_error(void);
+
+/* Synchronises `stream`, then reads and clears the device status word of the current
+ * device: QL_OK, QL_ERR_TIMEOUT if a bounded wait in a kernel ran out since the last
+ * check, or QL_ERR_CUDA if the synchronisation itself failed. */
+int qlinear_device_status(void *stream);
+
+/* Number of kernels one qlinear() call of this shape launches (for launch accounting);
+ * QL_ERR_* on invalid arguments. */
+int qlinear_launch_count(int type, int64_t N, int64_t K, int64_t M);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QLINEAR_H_ */

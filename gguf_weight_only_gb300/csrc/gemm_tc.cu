@@ -1,0 +1,555 @@
+// gemm_tc.cu -- prefill-path quantized linear y[M, N] = x[M, K] . dequant(W)[N, K]^T on the
+// 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// Tiling ("swap AB"): a CTA owns 128 weight rows (the MMA's M side, one TMEM lane per row)
+// and a tile of n_tile tokens (the MMA's N side, 32..256). The fp32 accumulator lives in
+// TMEM columns [0, n_tile). K is walked in chunks of 64 (four MMAs of K = 16).
+//
+// Warp roles (352 threads):
+//   warps 0-7  dequantisers: warp w serves TMEM lane quarter w % 4 (rows 32(w%4)..+31, one
+//              thread per row) and half w / 4 of every 64-wide chunk. Each thread decodes its
+//              row's 32 weights of the chunk from the staged superblock into fp16 and writes
+//              them with tcgen05.st into a TMEM A-operand ring (4 chunks x 32 columns); the
+//              MMA reads A straight from TMEM, so dequantised weights never touch shared
+//              memory. After the K loop the same warps drain the accumulator (tcgen05.ld) to y.
+//   warp 8     weight producer: bulk copies (TMA engine) of one superblock of the 128 rows
+//              into a shared-memory ring.
+//   warp 9     activation producer: 2-D TMA of the x tile [n_tile tokens x 64 k], 128-byte
+//              swizzled, the MMA's B operand.
+//   warp 10    TMEM allocator and the single MMA-issuing thread.
+// All hand-offs are mbarriers; every wait is bounded and an expired wait aborts the CTA
+// (status word set, TMEM freed).
+#include <cstdint>
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace ql {
+
+namespace {
+
+constexpr int kRows = 128;          // weight rows per CTA (MMA M)
+constexpr int kChunkK = 64;         // k per pipeline chunk
+constexpr int kAStages = 4;         // TMEM A ring depth (chunks)
+constexpr uint32_t kACol = 256;     // first TMEM column of the A ring
+constexpr int kDequantWarps = 8;
+constexpr int kThreads = 32 * 11;
+constexpr uint32_t kTmemCols = 512;
+
+struct GemmArgs {
+    const uint8_t *W;
+    float *y;
+    unsigned *status;
+    int N, K, M, nsb;
+    int n_tile;
+    uint32_t row_pitch;        // bytes per weight row in a quant stage
+    int qstages, bstages;
+    uint32_t q_stage_bytes, b_stage_bytes;
+    uint32_t q_off, bar_off;   // offsets from the 1024-aligned shared base
+    int64_t total_bytes;
+    int bb;                    // bytes per superblock
+    int type;
+};
+
+// ------------------------------------------------------------ per-row dequantisers
+// Each produces the 32 fp16 weights k = 32h .. 32h+31 of 64-wide chunk gg of one row as 16
+// packed pairs (k, k+1), i.e. the 16 TMEM columns [16h, 16h+16) of that chunk.
+
+struct KqRow {
+    uint32_t ds[4], ndm[4];   // (d*sc, .), (-dmin*m, .) of sub-blocks 2gg + h, gg = 0..3
+};
+
+__device__ __forceinline__ KqRow kq_row(uint32_t blk, int h) {
+    const uint4 hd = lds128(blk);
+    const uint32_t A = hd.y, B = hd.z, C = hd.w;
+    const uint32_t sc_lo4 = A & 0x3F3F3F3Fu, m_lo4 = B & 0x3F3F3F3Fu;
+    const uint32_t sc_hi4 = and_or(C, 0x0F0F0F0Fu, (A >> 2) & 0x30303030u);
+    const uint32_t m_hi4 = and_or(C >> 4, 0x0F0F0F0Fu, (B >> 2) & 0x30303030u);
+    // pool byte j = value of sub-block j; pick j = h, 2+h, 4+h, 6+h
+    const uint32_t sel = static_cast<uint32_t>(h) | ((2u + h) << 4) | ((4u + h) << 8) | ((6u + h) << 12);
+    const uint32_t sc4 = prmt(sc_lo4, sc_hi4, sel), m4 = prmt(m_lo4, m_hi4, sel);
+    const uint32_t d2 = prmt(hd.x, 0u, 0x1010u), dmin2 = prmt(hd.x, 0u, 0x3232u);   // (d, d), (dmin, dmin)
+    KqRow r;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t s = 0x4040u + 0x0101u * i;   // byte i, twice, with 0x64 high bytes
+        const uint32_t sc2 = hsub2(prmt(sc4, 0x64646464u, s), kH2_1024);
+        const uint32_t m2 = hsub2(prmt(m4, 0x64646464u, s), kH2_1024);
+        r.ds[i] = hmul2(d2, sc2);
+        r.ndm[i] = hmul2(dmin2, m2) ^ 0x80008000u;
+    }
+    return r;
+}
+
+template <bool Q5>
+__device__ __forceinline__ void kq_chunk(uint32_t blk, int gg, int h, const KqRow &r, uint32_t (&out)[16]) {
+    constexpr uint32_t QS = Q5 ? 48 : 16;
+    const uint4 q0 = lds128(blk + QS + 32 * gg), q1 = lds128(blk + QS + 32 * gg + 16);
+    uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
+    if constexpr (Q5) {
+        h0 = lds128(blk + 16);
+        h1 = lds128(blk + 32);
+    }
+    const uint32_t ds = r.ds[gg], ndm = r.ndm[gg];
+    const uint32_t j = 2u * gg + h;   // sub-block (and qh bit) of these weights
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const uint32_t w = u < 4 ? (u == 0 ? q0.x : u == 1 ? q0.y : u == 2 ? q0.z : q0.w)
+                                 : (u == 4 ? q1.x : u == 5 ? q1.y : u == 6 ? q1.z : q1.w);
+        const uint32_t w2 = prmt(w, 0u, 0x3120u), w3 = w2 >> 8;
+        uint32_t v01, v23, q01, q23;
+        if (h == 0) {
+            v01 = and_or(w2, 0x000F000Fu, kH2_1024);
+            v23 = and_or(w3, 0x000F000Fu, kH2_1024);
+        } else {
+            v01 = and_or(w2, 0x00F000F0u, kH2_1024);
+            v23 = and_or(w3, 0x00F000F0u, kH2_1024);
+        }
+        if constexpr (Q5) {
+            const uint32_t hw = u < 4 ? (u == 0 ? h0.x : u == 1 ? h0.y : u == 2 ? h0.z : h0.w)
+                                      : (u == 4 ? h1.x : u == 5 ? h1.y : u == 6 ? h1.z : h1.w);
+            const uint32_t hq2 = prmt(hw, 0u, 0x3120u), hq3 = hq2 >> 8;
+            // bit j of each qh byte -> bit 4 (low nibble path) or bit 8 (high nibble path, x16)
+            const uint32_t rot = ((h == 0 ? 4u : 8u) - j) & 31u;
+            const uint32_t mask = h == 0 ? 0x00100010u : 0x01000100u;
+            v01 = or_and(v01, rotl(hq2, rot), mask);
+            v23 = or_and(v23, rotl(hq3, rot), mask);
+        }
+        if (h == 0) {
+            q01 = hsub2(v01, kH2_1024);
+            q23 = hsub2(v23, kH2_1024);
+        } else {
+            q01 = hfma2(v01, kH2_1_16, kH2_m64);
+            q23 = hfma2(v23, kH2_1_16, kH2_m64);
+        }
+        out[2 * u] = hfma2(q01, ds, ndm);
+        out[2 * u + 1] = hfma2(q23, ds, ndm);
+    }
+}
+
+__device__ __forceinline__ uint4 lds128_a2(uint32_t addr) {
+    const uint32_t a = addr & ~3u;
+    const uint32_t sel = (addr & 2u) ? 0x5432u : 0x3210u;
+    const uint32_t w0 = lds32(a), w1 = lds32(a + 4), w2 = lds32(a + 8), w3 = lds32(a + 12), w4 = lds32(a + 16);
+    return make_uint4(prmt(w0, w1, sel), prmt(w1, w2, sel), prmt(w2, w3, sel), prmt(w3, w4, sel));
+}
+
+// Q6_K chunk gg: half hf = gg / 2 of the block, quarter t = 2 (gg % 2) + h, l = 0..31.
+__device__ __forceinline__ void q6_chunk(uint32_t blk, int gg, int h, uint32_t (&out)[16]) {
+    const int hf = gg >> 1, t = 2 * (gg & 1) + h;
+    const uint32_t d = lds16(blk + 208);
+    const uint32_t d2 = d | (d << 16);
+    const uint32_t scb = lds16(blk + 192 + 8 * hf + 2 * t) ^ 0x8080u;   // sc[8hf+2t], sc[8hf+2t+1] (+128)
+    const uint32_t kH2_1152 = 0x64806480u;
+    const uint32_t ds0 = hmul2(d2, hsub2(prmt(scb, 0x64646464u, 0x4040u), kH2_1152));   // l < 16
+    const uint32_t ds1 = hmul2(d2, hsub2(prmt(scb, 0x64646464u, 0x4141u), kH2_1152));   // l >= 16
+    const uint32_t qlo = 64 * hf + 32 * h, qho = 128 + 32 * hf;
+    const uint4 l0 = lds128_a2(blk + qlo), l1 = lds128_a2(blk + qlo + 16);
+    const uint4 g0 = lds128_a2(blk + qho), g1 = lds128_a2(blk + qho + 16);
+    const int sh = 4 - 2 * t;   // qh bits 2t, 2t+1 -> bits 4, 5
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const uint32_t lw = u < 4 ? (u == 0 ? l0.x : u == 1 ? l0.y : u == 2 ? l0.z : l0.w)
+                                  : (u == 4 ? l1.x : u == 5 ? l1.y : u == 6 ? l1.z : l1.w);
+        const uint32_t hw = u < 4 ? (u == 0 ? g0.x : u == 1 ? g0.y : u == 2 ? g0.z : g0.w)
+                                  : (u == 4 ? g1.x : u == 5 ? g1.y : u == 6 ? g1.z : g1.w);
+        uint32_t l2 = prmt(lw, 0u, 0x3120u);
+        if (t >= 2) l2 >>= 4;
+        const uint32_t l3 = l2 >> 8;
+        const uint32_t h2 = prmt(hw, 0u, 0x3120u), h3 = h2 >> 8;
+        uint32_t v01 = and_or(l2, 0x000F000Fu, kH2_1024);
+        uint32_t v23 = and_or(l3, 0x000F000Fu, kH2_1024);
+        v01 = or_and(v01, sh >= 0 ? (h2 << sh) : (h2 >> -sh), 0x00300030u);
+        v23 = or_and(v23, sh >= 0 ? (h3 << sh) : (h3 >> -sh), 0x00300030u);
+        const uint32_t ds = u < 4 ? ds0 : ds1;
+        out[2 * u] = hmul2(hsub2(v01, kH2_1056), ds);
+        out[2 * u + 1] = hmul2(hsub2(v23, kH2_1056), ds);
+    }
+}
+
+constexpr uint32_t kIq4T0 = 0x3F2D1801u, kIq4T1 = 0x766A5D4Fu, kIq4T2 = 0xA6998D81u, kIq4T3 = 0xF1D9C5B5u;
+
+__device__ __forceinline__ uint32_t iq4_lookup(uint32_t s) {
+    const uint32_t s7 = s & 0x7777u;
+    const uint32_t lo = prmt(kIq4T0, kIq4T1, s7), hi = prmt(kIq4T2, kIq4T3, s7);
+    return prmt(lo, hi, ((s >> 1) & 0x4444u) | 0x3210u);
+}
+
+// IQ4_XS chunk gg, half h: sub-block j = 2gg + h, 16 qs bytes -> [low nibbles, high nibbles].
+__device__ __forceinline__ void iq4_chunk(uint32_t blk, int gg, int h, uint32_t (&out)[16]) {
+    const int j = 2 * gg + h;
+    const uint2 hd = lds64(blk);
+    const uint32_t ls = ((hd.y >> (4 * j)) & 15u) | (((hd.x >> (16 + 2 * j)) & 3u) << 4);
+    const uint32_t d2 = prmt(hd.x, 0u, 0x1010u);
+    const uint32_t dl = hmul2(d2, hsub2(prmt(ls, 0x64646464u, 0x4040u), kH2_1056));   // d * (ls - 32)
+    const uint2 a = lds64(blk + 8 + 16 * j), b = lds64(blk + 16 + 16 * j);
+    const uint32_t kH2_1152 = 0x64806480u;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const uint32_t w = u == 0 ? a.x : u == 1 ? a.y : u == 2 ? b.x : b.y;   // bytes p = 4u .. 4u+3
+        const uint32_t r01 = iq4_lookup(w), r23 = iq4_lookup(w >> 16);
+        out[2 * u] = hmul2(hsub2(prmt(r01, 0x64646464u, 0x4240u), kH2_1152), dl);       // r = p, p+1
+        out[2 * u + 1] = hmul2(hsub2(prmt(r23, 0x64646464u, 0x4240u), kH2_1152), dl);   // p+2, p+3
+        out[8 + 2 * u] = hmul2(hsub2(prmt(r01, 0x64646464u, 0x4341u), kH2_1152), dl);   // p+16, p+17
+        out[9 + 2 * u] = hmul2(hsub2(prmt(r23, 0x64646464u, 0x4341u), kH2_1152), dl);   // p+18, p+19
+    }
+}
+
+// ------------------------------------------------------------ bounded waits with abort
+
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                              unsigned *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1u;
+            atomicOr(status, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
+}  // namespace
+
+template <int TYPE>
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *const gbase = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const uint32_t b_ring = base;
+    const uint32_t q_ring = base + p.q_off;
+    const uint32_t bars = base + p.bar_off;
+    const int QS = p.qstages, BS = p.bstages;
+    auto qfull = [&](int s) { return bars + 8u * s; };
+    auto qempty = [&](int s) { return bars + 8u * (QS + s); };
+    auto bfull = [&](int s) { return bars + 8u * (2 * QS + s); };
+    auto bempty = [&](int s) { return bars + 8u * (2 * QS + BS + s); };
+    auto afull = [&](int s) { return bars + 8u * (2 * QS + 2 * BS + s); };
+    auto aempty = [&](int s) { return bars + 8u * (2 * QS + 2 * BS + kAStages + s); };
+    const uint32_t accfull = bars + 8u * (2 * QS + 2 * BS + 2 * kAStages);
+    const uint32_t misc_off = p.bar_off + 8u * (2 * QS + 2 * BS + 2 * kAStages + 1);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + misc_off);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + misc_off + 4);
+
+    const int n0 = blockIdx.x * kRows;
+    const int t0 = blockIdx.y * p.n_tile;
+    const int nchunks = p.nsb * 4;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < QS; ++s) {
+            mbar_init(qfull(s), 1);
+            mbar_init(qempty(s), kDequantWarps);
+        }
+        for (int s = 0; s < BS; ++s) {
+            mbar_init(bfull(s), 1);
+            mbar_init(bempty(s), 1);
+        }
+        for (int s = 0; s < kAStages; ++s) {
+            mbar_init(afull(s), kDequantWarps);
+            mbar_init(aempty(s), 1);
+        }
+        mbar_init(accfull, 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 10) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 9 && lane == 0) prefetch_tmap(&xmap);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < kDequantWarps) {
+        // ---------------------------------------------------- dequantisers
+        const int q = warp & 3, h = warp >> 2;
+        const int r = 32 * q + lane;
+        const int row = min(n0 + r, p.N - 1);
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+        bool ok = true;
+        KqRow kr{};
+        uint32_t blk = 0;
+        for (int chunk = 0; chunk < nchunks && ok; ++chunk) {
+            const int sb = chunk >> 2, gg = chunk & 3;
+            const int qs = sb % QS;
+            if (gg == 0) {
+                ok = wait_or_abort(qfull(qs), (sb / QS) & 1, abort_flag, p.status);
+                if (!ok) break;
+                const int64_t o = (static_cast<int64_t>(row) * p.nsb + sb) * p.bb;
+                blk = q_ring + qs * p.q_stage_bytes + r * p.row_pitch + static_cast<uint32_t>(o & 15);
+                if constexpr (TYPE == 12 || TYPE == 13) kr = kq_row(blk, h);
+            }
+            const int sa = chunk % kAStages;
+            ok = wait_or_abort(aempty(sa), ((chunk / kAStages) & 1) ^ 1, abort_flag, p.status);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t out[16];
+            if constexpr (TYPE == 12) kq_chunk<false>(blk, gg, h, kr, out);
+            else if constexpr (TYPE == 13) kq_chunk<true>(blk, gg, h, kr, out);
+            else if constexpr (TYPE == 14) q6_chunk(blk, gg, h, out);
+            else iq4_chunk(blk, gg, h, out);
+            tmem_st16(tmem + lane_base + kACol + sa * 32 + 16 * h, out);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(afull(sa));
+                if (gg == 3) mbar_arrive(qempty(qs));
+            }
+        }
+        // ---------------------------------------------------- epilogue: TMEM -> y
+        if (ok) ok = wait_or_abort(accfull, 0, abort_flag, p.status);
+        if (ok) {
+            tc_fence_after();
+            const int half = p.n_tile / 2;
+            for (int c0 = h * half; c0 < (h + 1) * half; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld16(tmem + lane_base + c0, v);
+                tmem_wait_ld();
+                if (n0 + r < p.N) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int t = t0 + c0 + i;
+                        if (t < p.M) p.y[static_cast<int64_t>(t) * p.N + n0 + r] = __uint_as_float(v[i]);
+                    }
+                }
+            }
+        }
+    } else if (warp == 8) {
+        // ---------------------------------------------------- weight producer
+        int issued = 0;
+        for (int sb = 0; sb < p.nsb; ++sb) {
+            const int s = sb % QS;
+            if (!wait_or_abort(qempty(s), ((sb / QS) & 1) ^ 1, abort_flag, p.status)) break;
+            fence_proxy_async_smem();
+            const uint32_t st = q_ring + s * p.q_stage_bytes;
+            uint32_t my = 0;
+            const uint8_t *src[4];
+            uint32_t dst[4], nb[4];
+            int tail_len = 0;
+            uint32_t tail_dst = 0;
+            const uint8_t *tail_src = nullptr;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int rr = lane + 32 * i, rowi = n0 + rr;
+                nb[i] = 0;
+                src[i] = nullptr;
+                dst[i] = 0;
+                if (rowi < p.N) {
+                    const int64_t o = (static_cast<int64_t>(rowi) * p.nsb + sb) * p.bb;
+                    const int64_t lo = o & ~int64_t(15);
+                    int64_t hi = (o + p.bb + 15) & ~int64_t(15);
+                    const int64_t t16 = p.total_bytes & ~int64_t(15);
+                    if (hi > t16) {
+                        hi = t16;
+                        tail_len = static_cast<int>(o + p.bb - t16);
+                        tail_src = p.W + t16;
+                        tail_dst = st + rr * p.row_pitch + static_cast<uint32_t>(t16 - lo);
+                    }
+                    src[i] = p.W + lo;
+                    dst[i] = st + rr * p.row_pitch;
+                    nb[i] = static_cast<uint32_t>(hi - lo);
+                }
+                my += nb[i];
+            }
+            if (tail_len > 0) {
+                uint8_t *gd = gbase + (tail_dst - base);
+                for (int i = 0; i < tail_len; ++i) gd[i] = __ldg(tail_src + i);
+            }
+            const uint32_t total = __reduce_add_sync(0xFFFFFFFFu, my);
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(qfull(s), total);
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (nb[i]) bulk_g2s(dst[i], src[i], nb[i], qfull(s));
+            issued = sb + 1;
+        }
+        if (*abort_flag) {   // let issued copies land before the CTA's shared memory is released
+            for (int sb = max(0, issued - QS); sb < issued; ++sb) (void)mbar_wait(qfull(sb % QS), (sb / QS) & 1);
+        }
+    } else if (warp == 9) {
+        // ---------------------------------------------------- activation producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int chunk = 0; chunk < nchunks; ++chunk) {
+                const int s = chunk % BS;
+                if (!wait_or_abort(bempty(s), ((chunk / BS) & 1) ^ 1, abort_flag, p.status)) break;
+                mbar_arrive_expect_tx(bfull(s), p.b_stage_bytes);
+                tma_load_2d(b_ring + s * p.b_stage_bytes, &xmap, chunk * kChunkK, t0, bfull(s));
+                issued = chunk + 1;
+            }
+            if (*abort_flag) {
+                for (int c = max(0, issued - BS); c < issued; ++c) (void)mbar_wait(bfull(c % BS), (c / BS) & 1);
+            }
+        }
+    } else {
+        // ---------------------------------------------------- MMA issuer (warp 10)
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16_f32(kRows, p.n_tile);
+            bool ok = true;
+            for (int chunk = 0; chunk < nchunks; ++chunk) {
+                const int sa = chunk % kAStages, sbb = chunk % BS;
+                if (!wait_or_abort(afull(sa), (chunk / kAStages) & 1, abort_flag, p.status) ||
+                    !wait_or_abort(bfull(sbb), (chunk / BS) & 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t bst = b_ring + sbb * p.b_stage_bytes;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc_mma_ts(tmem, tmem + kACol + sa * 32 + kk * 8, smem_desc_sw128(bst + 32 * kk), idesc,
+                              (chunk | kk) != 0);
+                tc_commit(aempty(sa));
+                tc_commit(bempty(sbb));
+            }
+            tc_commit(accfull);   // also drains in-flight MMAs on the abort path
+            if (!ok) (void)mbar_wait(accfull, 0);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 10) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------------ host side
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+int pick_n_tile(int64_t M) {
+    if (M >= 256) return 256;
+    int n = static_cast<int>((M + 31) / 32) * 32;
+    return n < 32 ? 32 : n;
+}
+
+struct GemmPlan {
+    int n_tile, qstages, bstages;
+    uint32_t row_pitch, q_stage_bytes, b_stage_bytes, q_off, bar_off;
+    size_t smem;
+};
+
+GemmPlan gemm_plan(int bb, int64_t M) {
+    GemmPlan pl{};
+    pl.n_tile = pick_n_tile(M);
+    // window of one superblock incl. misalignment, rounded to an odd multiple of 16 bytes
+    uint32_t pitch = static_cast<uint32_t>((bb % 16 == 0) ? bb : ((bb + 30) & ~15));
+    if ((pitch / 16) % 2 == 0) pitch += 16;
+    pl.row_pitch = pitch;
+    pl.q_stage_bytes = kRows * pitch;
+    pl.b_stage_bytes = static_cast<uint32_t>(pl.n_tile) * 128u;
+    const size_t limit = 227 * 1024 - 1024;
+    for (int bs = 4; bs >= 2; --bs) {
+        for (int qs = 3; qs >= 2; --qs) {
+            const size_t q_off = static_cast<size_t>(bs) * pl.b_stage_bytes;
+            const size_t bar_off = q_off + static_cast<size_t>(qs) * pl.q_stage_bytes;
+            const size_t total = bar_off + 8 * (2 * qs + 2 * bs + 2 * kAStages + 1) + 16;
+            if (total <= limit) {
+                pl.bstages = bs;
+                pl.qstages = qs;
+                pl.q_off = static_cast<uint32_t>(q_off);
+                pl.bar_off = static_cast<uint32_t>(bar_off);
+                pl.smem = total + 1024;   // slack for 1024-byte alignment of the base
+                return pl;
+            }
+        }
+    }
+    pl.n_tile = 0;
+    return pl;
+}
+
+template <int TYPE>
+cudaError_t launch_t(const CUtensorMap &xmap, const GemmArgs &a, dim3 grid, size_t smem, cudaStream_t st) {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<TYPE>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    gemm_kernel<TYPE><<<grid, kThreads, smem, st>>>(xmap, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_launch_count(int, int64_t, int64_t, int64_t) { return 1; }
+
+cudaError_t gemm_launch(int type, const uint8_t *W, const __half *x, float *y, int64_t N, int64_t K, int64_t M,
+                        unsigned *status, int, cudaStream_t stream) {
+    const int bb = gemv_block_bytes(type);
+    if (bb < 0) return cudaErrorInvalidValue;
+    const GemmPlan pl = gemm_plan(bb, M);
+    if (pl.n_tile == 0) return cudaErrorNotSupported;
+    auto enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+
+    CUtensorMap xmap;
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kChunkK), static_cast<cuuint32_t>(pl.n_tile)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult cr = enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half *>(x), gdim, gstride, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+
+    GemmArgs a{};
+    a.W = W;
+    a.y = y;
+    a.status = status;
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.M = static_cast<int>(M);
+    a.nsb = static_cast<int>(K / 256);
+    a.n_tile = pl.n_tile;
+    a.row_pitch = pl.row_pitch;
+    a.qstages = pl.qstages;
+    a.bstages = pl.bstages;
+    a.q_stage_bytes = pl.q_stage_bytes;
+    a.b_stage_bytes = pl.b_stage_bytes;
+    a.q_off = pl.q_off;
+    a.bar_off = pl.bar_off;
+    a.total_bytes = N * (K / 256) * bb;
+    a.bb = bb;
+    a.type = type;
+    const dim3 grid(static_cast<unsigned>((N + kRows - 1) / kRows), static_cast<unsigned>((M + pl.n_tile - 1) / pl.n_tile));
+    switch (type) {
+    case 12: return launch_t<12>(xmap, a, grid, pl.smem, stream);
+    case 13: return launch_t<13>(xmap, a, grid, pl.smem, stream);
+    case 14: return launch_t<14>(xmap, a, grid, pl.smem, stream);
+    case 23: return launch_t<23>(xmap, a, grid, pl.smem, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace ql

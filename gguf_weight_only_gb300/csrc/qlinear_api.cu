@@ -1,0 +1,165 @@
+// qlinear_api.cu -- the C ABI declared in include/qlinear.h: argument validation, per-device
+// state, and dispatch on M between the decode GEMV and the tcgen05 prefill GEMM.
+#include <cstdint>
+#include <mutex>
+
+#include "kernels.h"
+#include "qlinear.h"
+
+namespace {
+
+// Device status word: kernels OR error bits into it (a bounded wait that ran out).
+__device__ unsigned g_status_word;
+
+struct DeviceState {
+    bool ready = false;
+    int status = QL_OK;       // QL_OK or the error of the failed initialisation
+    int num_sms = 0;
+    unsigned *status_word = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceState g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+thread_local int t_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+    t_last_cuda_error = static_cast<int>(e);
+    return QL_ERR_CUDA;
+}
+
+// Per-device one-time set-up (SM count, sm_103 check, status-word address), done with
+// the device current. Returns QL_OK or an error.
+int device_state(DeviceState **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return QL_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceState &s = g_dev[dev];
+    if (!s.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e);
+        if (major != 10 || minor != 3) {
+            s.status = QL_ERR_DEVICE;
+        } else {
+            void *p = nullptr;
+            if ((e = cudaGetSymbolAddress(&p, g_status_word)) != cudaSuccess) return cuda_fail(e);
+            s.status_word = static_cast<unsigned *>(p);
+            s.num_sms = sms;
+            s.status = QL_OK;
+        }
+        s.ready = true;
+    }
+    *out = &s;
+    return s.status;
+}
+
+int validate(int type, const void *W, int64_t N, int64_t K, const void *x, int64_t M, const float *y) {
+    if (ql::gemv_block_bytes(type) < 0) return QL_ERR_TYPE;
+    if (N < 1 || M < 1 || K < 256 || K % 256 != 0) return QL_ERR_SHAPE;
+    // 32-bit indexing limits inside the kernels
+    if (N > (int64_t(1) << 30) || K > (int64_t(1) << 24) || M > (int64_t(1) << 24)) return QL_ERR_SHAPE;
+    if (M * K > (int64_t(1) << 40) || M * N > (int64_t(1) << 40)) return QL_ERR_SHAPE;
+    if (!W || !x || !y) return QL_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(W) | reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u)
+        return QL_ERR_ALIGN;
+    return QL_OK;
+}
+
+enum class Path { Auto, Gemv, Gemm };
+
+int run_gemv(const DeviceState &s, int type, const void *W, int64_t N, int64_t K, const void *x, int64_t M, float *y,
+             cudaStream_t st) {
+    // tokens in groups of kGemvMaxM: one launch per group (the weights stream once per group)
+    for (int64_t m0 = 0; m0 < M; m0 += ql::kGemvMaxM) {
+        const int mg = static_cast<int>(M - m0 < ql::kGemvMaxM ? M - m0 : ql::kGemvMaxM);
+        cudaError_t e = ql::gemv_launch(type, static_cast<const uint8_t *>(W),
+                                        static_cast<const __half *>(x) + m0 * K, y + m0 * N, N, K, mg,
+                                        s.status_word, s.num_sms, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return QL_OK;
+}
+
+int run(Path path, int type, const void *W, int64_t N, int64_t K, const void *x, int64_t M, float *y, void *stream) {
+    int rc = validate(type, W, N, K, x, M, y);
+    if (rc != QL_OK) return rc;
+    DeviceState *s = nullptr;
+    if ((rc = device_state(&s)) != QL_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (path == Path::Gemv || (path == Path::Auto && M <= ql::kGemvMaxM))
+        return run_gemv(*s, type, W, N, K, x, M, y, st);
+    cudaError_t e = ql::gemm_launch(type, static_cast<const uint8_t *>(W), static_cast<const __half *>(x), y, N, K, M,
+                                    s->status_word, s->num_sms, st);
+    if (e == cudaErrorNotSupported) return QL_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return cuda_fail(e);
+    return QL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qlinear(int type, const void *W_blocks, int64_t N, int64_t K, const void *x_fp16, int64_t M, float *y_fp32,
+            void *stream) {
+    return run(Path::Auto, type, W_blocks, N, K, x_fp16, M, y_fp32, stream);
+}
+
+int qlinear_gemv(int type, const void *W_blocks, int64_t N, int64_t K, const void *x_fp16, int64_t M, float *y_fp32,
+                 void *stream) {
+    return run(Path::Gemv, type, W_blocks, N, K, x_fp16, M, y_fp32, stream);
+}
+
+int qlinear_gemm(int type, const void *W_blocks, int64_t N, int64_t K, const void *x_fp16, int64_t M, float *y_fp32,
+                 void *stream) {
+    return run(Path::Gemm, type, W_blocks, N, K, x_fp16, M, y_fp32, stream);
+}
+
+int qlinear_block_bytes(int type) {
+    const int b = ql::gemv_block_bytes(type);
+    return b < 0 ? QL_ERR_TYPE : b;
+}
+
+int qlinear_gemv_max_m(void) { return ql::kGemvMaxM; }
+
+const char *qlinear_strerror(int status) {
+    switch (status) {
+    case QL_OK: return "success";
+    case QL_ERR_TYPE: return "unsupported ggml type (expected Q4_K=12, Q5_K=13, Q6_K=14, IQ4_XS=23)";
+    case QL_ERR_SHAPE: return "bad shape (need K % 256 == 0, K >= 256, N >= 1, M >= 1, within 32-bit indexing)";
+    case QL_ERR_NULL: return "null pointer argument";
+    case QL_ERR_ALIGN: return "W, x and y must be 16-byte aligned";
+    case QL_ERR_CUDA: return "CUDA runtime error (see qlinear_last_cuda_error)";
+    case QL_ERR_TIMEOUT: return "a device-side bounded wait ran out";
+    case QL_ERR_UNSUPPORTED: return "the requested kernel cannot run this shape";
+    case QL_ERR_DEVICE: return "current device is not an sm_103 (GB300) GPU";
+    default: return "unknown status";
+    }
+}
+
+int qlinear_last_cuda_error(void) { return t_last_cuda_error; }
+
+int qlinear_device_status(void *stream) {
+    DeviceState *s = nullptr;
+    int rc = device_state(&s);
+    if (rc != QL_OK) return rc;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    unsigned word = 0, zero = 0;
+    if ((e = cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word))) != cudaSuccess) return cuda_fail(e);
+    if (word != 0 && (e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero))) != cudaSuccess) return cuda_fail(e);
+    return word ? QL_ERR_TIMEOUT : QL_OK;
+}
+
+int qlinear_launch_count(int type, int64_t N, int64_t K, int64_t M) {
+    if (ql::gemv_block_bytes(type) < 0) return QL_ERR_TYPE;
+    if (N < 1 || M < 1 || K < 256 || K % 256 != 0) return QL_ERR_SHAPE;
+    if (M <= ql::kGemvMaxM) return 1;
+    return ql::gemm_launch_count(type, N, K, M);
+}
+
+}  // extern "C"

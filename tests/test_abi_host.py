@@ -1,0 +1,87 @@
+"""Host-side checks of the C ABI (no GPU): the library builds and loads, exports every
+function include/qlinear.h declares, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import gguf_weight_only_gb300 as ql
+from gguf_weight_only_gb300 import build as qbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qlinear.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    qbuild.build()
+    return ql.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(?:int|const char\s*\*|void)\s*\*?\s*(qlinear\w*)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_lists_match_binding():
+    assert declared_functions() == sorted(ql.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", qbuild.LIB], capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_block_bytes_and_metadata(lib):
+    assert [ql.block_bytes(t) for t in (12, 13, 14, 23)] == [144, 176, 210, 136]
+    assert ql.block_bytes(2) == -1
+    assert ql.gemv_max_m() == 8
+    for s in range(-8, 1):
+        assert isinstance(ql.strerror(s), str) and ql.strerror(s)
+    assert ql.strerror(-99) == "unknown status"
+    assert lib.qlinear_last_cuda_error() == 0
+
+
+def test_launch_count(lib):
+    assert ql.launch_count(12, 4096, 4096, 1) == 1
+    assert ql.launch_count(12, 4096, 4096, 8) == 1
+    assert ql.launch_count(12, 12288, 4096, 512) == 1
+    assert ql.launch_count(12, 4096, 100, 1) == -2
+    assert ql.launch_count(99, 4096, 4096, 1) == -1
+
+
+BAD = [
+    # (type, W, N, K, x, M, y, expected)
+    (7, 16, 8, 256, 16, 1, 16, -1),          # unsupported type
+    (12, 16, 8, 300, 16, 1, 16, -2),         # K not a multiple of 256
+    (12, 16, 0, 256, 16, 1, 16, -2),         # N < 1
+    (12, 16, 8, 256, 16, 0, 16, -2),         # M < 1
+    (12, 16, 8, 0, 16, 1, 16, -2),           # K = 0
+    (12, 0, 8, 256, 16, 1, 16, -3),          # null W
+    (12, 16, 8, 256, 0, 1, 16, -3),          # null x
+    (12, 16, 8, 256, 16, 1, 0, -3),          # null y
+    (12, 24, 8, 256, 16, 1, 16, -4),         # misaligned W
+    (12, 16, 8, 256, 40, 1, 16, -4),         # misaligned x
+    (12, 16, 8, 256, 16, 1, 20, -4),         # misaligned y
+]
+
+
+@pytest.mark.parametrize("fn", ["qlinear", "qlinear_gemv", "qlinear_gemm"])
+@pytest.mark.parametrize("case", BAD)
+def test_bad_arguments_rejected_before_launch(lib, fn, case):
+    t, W, N, K, x, M, y, expect = case
+    f = getattr(lib, fn)
+    assert f(t, ctypes.c_void_p(W or None), N, K, ctypes.c_void_p(x or None), M, ctypes.c_void_p(y or None), None) == expect
+
+
+def test_python_wrapper_raises_without_cuda_tensors(lib):
+    import torch
+    with pytest.raises(TypeError):
+        ql.qlinear(torch.zeros(144, dtype=torch.uint8), 12, 1, 256, torch.zeros(1, 256, dtype=torch.float16))

@@ -1,0 +1,171 @@
+"""GPU parity: the CUDA kernels (through the C ABI) against the fp64 oracle, element by
+element, with the stated tolerance |y - y_oracle| <= 2e-3 * sum_k |x_k * w_k|."""
+import numpy as np
+import pytest
+
+import oracle
+from gguf_weight_only_gb300 import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+TYPES = (12, 13, 14, 23)
+
+
+@pytest.fixture(scope="module")
+def ql():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gguf_weight_only_gb300 import build
+    build.build()
+    import gguf_weight_only_gb300 as q
+    q.lib()
+    return q
+
+
+def run(ql, path, t, W, N, K, x):
+    Wd = torch.from_numpy(W).cuda()
+    xd = torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    y = ql.qlinear(Wd, t, N, K, xd, path=path)
+    torch.cuda.synchronize()
+    assert ql.device_status() == 0
+    return y.cpu().numpy().astype(np.float64)
+
+
+def check(y, ref, tol, what):
+    assert y.shape == ref.shape, what
+    assert np.all(np.isfinite(y)), what
+    err = np.abs(y - ref)
+    bad = err > tol
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside tolerance; first {tuple(i)} "
+                             f"y={y[tuple(i)]} ref={ref[tuple(i)]} tol={tol[tuple(i)]} max_ratio={np.max(err / np.maximum(tol, 1e-300))}")
+
+
+# ------------------------------------------------------------------ small / ragged shapes, both kernels
+
+GEMV_SHAPES = [(1, 256, 1), (7, 512, 3), (13, 1024, 8), (37, 768, 2), (129, 2560, 5), (300, 5120, 1), (64, 4096, 4)]
+
+
+@pytest.mark.parametrize("t", TYPES)
+@pytest.mark.parametrize("N,K,M", GEMV_SHAPES)
+def test_gemv_matches_oracle(ql, t, N, K, M):
+    W = synth.weights(t, N, K, [100, t, N, K])
+    x = synth.activations(M, K, [101, t, M, K])
+    ref = oracle.qlinear(t, W, N, K, x)
+    check(run(ql, "gemv", t, W, N, K, x), ref, oracle.tolerance(t, W, N, K, x), f"gemv t={t} N={N} K={K} M={M}")
+
+
+GEMM_SHAPES = [(128, 256, 32), (129, 512, 9), (300, 1024, 33), (1, 256, 1), (256, 2048, 100), (200, 768, 256),
+               (130, 1280, 300), (128, 512, 512)]
+
+
+@pytest.mark.parametrize("t", TYPES)
+@pytest.mark.parametrize("N,K,M", GEMM_SHAPES)
+def test_gemm_matches_oracle(ql, t, N, K, M):
+    W = synth.weights(t, N, K, [200, t, N, K])
+    x = synth.activations(M, K, [201, t, M, K])
+    ref = oracle.qlinear(t, W, N, K, x)
+    check(run(ql, "gemm", t, W, N, K, x), ref, oracle.tolerance(t, W, N, K, x), f"gemm t={t} N={N} K={K} M={M}")
+
+
+@pytest.mark.parametrize("t", TYPES)
+@pytest.mark.parametrize("M", [1, 8, 9, 64])
+def test_auto_dispatch_matches_oracle(ql, t, M):
+    N, K = 160, 1024
+    W = synth.weights(t, N, K, [300, t])
+    x = synth.activations(M, K, [301, t, M])
+    ref = oracle.qlinear(t, W, N, K, x)
+    check(run(ql, "auto", t, W, N, K, x), ref, oracle.tolerance(t, W, N, K, x), f"auto t={t} M={M}")
+
+
+@pytest.mark.parametrize("t", TYPES)
+def test_gemv_many_tokens_in_groups(ql, t):
+    """The forced decode kernel handles M > 8 as groups of 8 tokens."""
+    N, K, M = 40, 512, 19
+    W = synth.weights(t, N, K, [310, t])
+    x = synth.activations(M, K, [311, t])
+    ref = oracle.qlinear(t, W, N, K, x)
+    check(run(ql, "gemv", t, W, N, K, x), ref, oracle.tolerance(t, W, N, K, x), f"gemv groups t={t}")
+
+
+# ------------------------------------------------------------------ edge cases
+
+@pytest.mark.parametrize("path", ["gemv", "gemm"])
+@pytest.mark.parametrize("t", TYPES)
+def test_zero_weights_and_zero_activations(ql, path, t):
+    N, K, M = 33, 512, 3
+    W = synth.weights(t, N, K, [400, t])
+    x = np.zeros((M, K), np.float16)
+    y = run(ql, path, t, W, N, K, x)
+    assert np.all(y == 0.0)
+    Wz = np.zeros_like(W)                     # d = dmin = 0: every weight 0
+    x = synth.activations(M, K, [401, t])
+    assert np.all(run(ql, path, t, Wz, N, K, x) == 0.0)
+
+
+@pytest.mark.parametrize("t", TYPES)
+def test_unit_activation_picks_a_column(ql, t):
+    """x = e_k: the decode kernel returns column k of dequant(W). It multiplies exact
+    integer-valued fp16 operands and scales in fp32, so the only error is fp32 rounding."""
+    N, K = 70, 768
+    W = synth.weights(t, N, K, [410, t])
+    w = oracle.dequant(t, W, N, K)
+    ks = [0, 1, 255, 256, 511, 767]
+    x = np.zeros((len(ks), K), np.float16)
+    for i, k in enumerate(ks):
+        x[i, k] = 1.0
+    y = run(ql, "gemv", t, W, N, K, x)
+    ref = w[:, ks].T
+    np.testing.assert_allclose(y, ref, rtol=2 ** -20, atol=2 ** -40)
+
+
+@pytest.mark.parametrize("path", ["gemv", "gemm"])
+@pytest.mark.parametrize("t", TYPES)
+def test_deterministic(ql, path, t):
+    N, K, M = 257, 2048, 6 if path == "gemv" else 48
+    W = synth.weights(t, N, K, [420, t])
+    x = synth.activations(M, K, [421, t])
+    a = run(ql, path, t, W, N, K, x)
+    b = run(ql, path, t, W, N, K, x)
+    assert np.array_equal(a.view(np.uint64), b.view(np.uint64))
+
+
+@pytest.mark.parametrize("t", TYPES)
+def test_unaligned_source_copied_by_wrapper(ql, t):
+    """The pages store W at a 68-byte offset (test_llm_quant_cpu.py); the ABI rejects an
+    unaligned pointer and an aligned copy gives the oracle's result."""
+    N, K, M = 64, 256, 1
+    W = synth.weights(t, N, K, [430, t])
+    x = synth.activations(M, K, [431, t])
+    store = torch.from_numpy(np.concatenate([np.zeros(68, np.uint8), W])).cuda()
+    view = store[68:]
+    with pytest.raises(ql.QLinearError) as e:
+        ql.qlinear(view, t, N, K, torch.from_numpy(x).cuda())
+    assert e.value.status == -4
+    y = ql.qlinear(view.clone(), t, N, K, torch.from_numpy(x).cuda())
+    torch.cuda.synchronize()
+    check(y.cpu().numpy().astype(np.float64), oracle.qlinear(t, W, N, K, x), oracle.tolerance(t, W, N, K, x), "offset")
+
+
+# ------------------------------------------------------------------ full-size workloads, sampled rows
+
+FULL = [
+    (12, 4096, 4096, 1), (12, 4096, 1024, 4), (12, 4096, 12288, 1), (12, 12288, 4096, 4),
+    (23, 5120, 5120, 1), (23, 5120, 17408, 1), (23, 17408, 5120, 1),
+    (12, 4096, 12288, 32), (12, 4096, 12288, 128), (12, 4096, 12288, 512),
+    (13, 5120, 17408, 1), (13, 5120, 17408, 256), (14, 5120, 17408, 1), (14, 5120, 17408, 256),
+]
+
+
+@pytest.mark.parametrize("t,K,N,M", FULL)
+def test_full_size_sampled_rows(ql, t, K, N, M):
+    W = synth.weights(t, N, K, [500, t, K, N])
+    x = synth.activations(M, K, [501, t, M])
+    y = run(ql, "auto", t, W, N, K, x)
+    rng = np.random.default_rng(502)
+    rows = np.unique(np.concatenate([[0, 1, N - 1, N // 2], rng.choice(N, 60, replace=False)]))
+    ref = oracle.qlinear_rows(t, W, N, K, x, rows)
+    tol = oracle.tolerance_rows(t, W, N, K, x, rows)
+    check(y[:, rows], ref, tol, f"full t={t} K={K} N={N} M={M}")

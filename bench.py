@@ -1,0 +1,377 @@
+"""Benchmark of the GGUF weight-only quantized linear layer on GB300.
+
+One step = one decode pass over the linear layers of an 8B-class dense transformer layer:
+Q4_K weights, M = 1 token, (K, N) in (4096, 4096), (4096, 1024), (4096, 12288), (12288, 4096)
+-- four qlinear() calls. `value` is the whole job's algorithmic HBM throughput (quantized weight
+bytes + fp16 activations + fp32 outputs) in GB/s, with inputs resident in HBM. The step
+rotates over several copies of the weights (more than 2x the L2 size in total) so that no
+step finds its weights in L2. The prefill figure (TFLOP/s of the Q4_K K=4096, N=12288, M=512
+GEMM) and the dominant kernels' roofline fractions ride along in the same JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on this machine's cores (a deliberately slow
+baseline) on a bounded sample of the same workload.
+Multi-GPU (torchrun): every rank runs an independent replica of the workload (the layer has
+no exchange step); value sums the ranks' work over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gguf_weight_only_gb300 import synth  # noqa: E402
+
+DECODE_TYPE = 12
+DECODE_M = 1
+DECODE_SHAPES = synth.DECODE_8B_SHAPES                 # (K, N)
+PREFILL = (12, 4096, 12288, 512)                       # type, K, N, M
+METRIC = "qlinear weight GB/s (M=1) & TFLOP/s (M=512), % of HBM / FP16 roofline"
+BB = synth.BLOCK_BYTES
+
+
+def alg_bytes(t, K, N, M):
+    return N * (K // 256) * BB[t] + 2 * M * K + 4 * M * N
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gguf_weight_only_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernels."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    v = d.get("kernels", {}).get(kernel_key)
+    return None if v is None else float(v)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed region runs."""
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.rows, self.proc = index, [], None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 6:
+                self.rows.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[2 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# ---------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import gguf_weight_only_gb300 as ql
+    from gguf_weight_only_gb300 import build
+
+    if rank == 0 or not os.path.exists(build.LIB):
+        build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    lib = ql.lib()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    hbm, tf_burst, tf_sust, peak_kind = peaks()
+
+    # ---- inputs resident in HBM: P copies of the layer's weights, > 2x L2 in total
+    layer_bytes = sum(N * (K // 256) * BB[DECODE_TYPE] for K, N in DECODE_SHAPES)
+    P = max(2, int(np.ceil(2.2 * l2 / layer_bytes)))
+    base = [torch.from_numpy(synth.weights(DECODE_TYPE, N, K, synth.workload_seed(1, i))).to(dev)
+            for i, (K, N) in enumerate(DECODE_SHAPES)]
+    copies = [[b.clone() for b in base] for _ in range(P)]
+    xs = [torch.from_numpy(synth.activations(DECODE_M, K, synth.activation_seed(1, i, DECODE_M))).to(dev)
+          for i, (K, N) in enumerate(DECODE_SHAPES)]
+    ys = [torch.empty((DECODE_M, N), dtype=torch.float32, device=dev) for K, N in DECODE_SHAPES]
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+
+    def step(i):
+        Ws = copies[i % P]
+        for j, (K, N) in enumerate(DECODE_SHAPES):
+            rc = lib.qlinear(DECODE_TYPE, Ws[j].data_ptr(), N, K, xs[j].data_ptr(), DECODE_M, ys[j].data_ptr(), sh)
+            if rc != 0:
+                raise RuntimeError(f"qlinear failed: {ql.strerror(rc)}")
+
+    launches_per_step = sum(lib.qlinear_launch_count(DECODE_TYPE, N, K, DECODE_M) for K, N in DECODE_SHAPES)
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            step(i)
+    torch.cuda.synchronize(dev)
+
+    # Capture the K timed steps as one CUDA graph (launch-bound otherwise: a decode GEMV
+    # is a few microseconds); replay it once untimed, then time one replay.
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(args.steps):
+            step(i)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clk:
+        time.sleep(0.05)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    ms_total = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    step_bytes = sum(alg_bytes(DECODE_TYPE, K, N, DECODE_M) for K, N in DECODE_SHAPES)
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    if ys[2].isnan().any():
+        raise RuntimeError("NaN in output")
+    del g
+
+    # ---- dominant decode kernel alone: largest shape, CUDA-event time per launch
+    def time_kernel(t, K, N, M, path_fn, reps):
+        wb = N * (K // 256) * BB[t]
+        Pk = max(2, int(np.ceil(2.2 * l2 / wb)))
+        W0 = torch.from_numpy(synth.weights(t, N, K, [7, t, K, N])).to(dev)
+        Wk = [W0.clone() for _ in range(Pk)]
+        x = torch.from_numpy(synth.activations(M, K, [8, t, M])).to(dev)
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                path_fn(t, Wk[i % Pk].data_ptr(), N, K, x.data_ptr(), M, y.data_ptr(), sh)
+        torch.cuda.synchronize(dev)
+        gk = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gk, stream=stream):
+            for i in range(reps):
+                path_fn(t, Wk[i % Pk].data_ptr(), N, K, x.data_ptr(), M, y.data_ptr(), sh)
+        with torch.cuda.stream(stream):
+            gk.replay()
+        torch.cuda.synchronize(dev)
+        best = []
+        for _ in range(3):
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                gk.replay()
+                e1.record(stream)
+            torch.cuda.synchronize(dev)
+            best.append(e0.elapsed_time(e1) / reps)
+        del gk, Wk
+        torch.cuda.empty_cache()
+        return float(np.median(best))
+
+    Kd, Nd = DECODE_SHAPES[2]
+    ms_dec = time_kernel(DECODE_TYPE, Kd, Nd, DECODE_M, lib.qlinear, 200)
+    dec_bytes = alg_bytes(DECODE_TYPE, Kd, Nd, DECODE_M)
+    dec_gbs = dec_bytes / (ms_dec * 1e-3) / 1e9
+    t, Kp, Np, Mp = PREFILL
+    ms_pre = time_kernel(t, Kp, Np, Mp, lib.qlinear, 40)
+    pre_tf = 2.0 * Mp * Np * Kp / (ms_pre * 1e-3) / 1e12
+
+    # ---- end to end through the public Python API with host buffers
+    import gguf_weight_only_gb300 as qlp
+    x_host = [torch.from_numpy(synth.activations(DECODE_M, K, [9, i])).pin_memory() for i, (K, N) in enumerate(DECODE_SHAPES)]
+    y_host = [torch.empty((DECODE_M, N), dtype=torch.float32).pin_memory() for K, N in DECODE_SHAPES]
+    x_dev = [torch.empty((DECODE_M, K), dtype=torch.float16, device=dev) for K, N in DECODE_SHAPES]
+    h2d = sum(x.numel() * 2 for x in x_host)
+    d2h = sum(y.numel() * 4 for y in y_host)
+
+    def e2e_step(i):
+        Ws = copies[i % P]
+        for j, (K, N) in enumerate(DECODE_SHAPES):
+            x_dev[j].copy_(x_host[j], non_blocking=True)
+            qlp.qlinear(Ws[j], DECODE_TYPE, N, K, x_dev[j], out=ys[j])
+            y_host[j].copy_(ys[j], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            e2e_step(i)
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            e2e_step(i)
+        e2e_s = (time.perf_counter() - t0) / args.steps
+    e2e_val = world * step_bytes / e2e_s / 1e9
+
+    result = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp16 x, Q4_K weights, fp32 accumulate",
+        "data": "synthetic (seeded blocks and N(0,1) activations of the stated shapes)",
+        "config": {"workload": "Q4_K decode, 8B-class layer: M=1, (K,N) in (4096,4096),(4096,1024),(4096,12288),(12288,4096)",
+                   "weight_copies_rotated": P, "l2_bytes": l2,
+                   "l2_policy": f"inputs larger than L2: {P} rotated weight copies, {P * layer_bytes / 1e6:.0f} MB",
+                   "parallelism": f"replicas x{world}"},
+        "prefill": {"workload": "Q4_K GEMM K=4096 N=12288 M=512", "ms": round(ms_pre, 4),
+                    "tflops": round(pre_tf, 1), "peak_tflops": tf_burst, "frac": round(pre_tf / tf_burst, 4),
+                    "bound": "tensor"},
+        "roofline": {"bound": "hbm", "kernel": "gemv_kernel<12> K=4096 N=12288 M=1",
+                     "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(dec_gbs / hbm, 4), "peak_kind": peak_kind,
+                     "traffic": ncu_traffic("gemv_q4k_k4096_n12288_m1")},
+        "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * launches_per_step,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1:
+        result["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
+    return result
+
+
+# ---------------------------------------------------------------------------- oracle on the CPU
+
+def cpu_baseline(budget_s=12.0):
+    """The fp64 oracle (C, one POSIX thread per core) on a bounded sample of the decode
+    workload: the first rows of each layer shape, scaled to GB/s of that sample."""
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    total_bytes, total_s, rows_used = 0, 0.0, []
+    for i, (K, N) in enumerate(DECODE_SHAPES):
+        rows = max(cores, 64)
+        W = synth.weights(DECODE_TYPE, rows, K, [11, i])
+        x = synth.activations(DECODE_M, K, [12, i])
+        t0 = time.perf_counter()
+        oracle.qlinear(DECODE_TYPE, W, rows, K, x, n_threads=cores)
+        dt = time.perf_counter() - t0
+        # grow the sample to roughly budget/4 seconds per shape
+        rows = int(min(N, max(rows, rows * (budget_s / 4) / max(dt, 1e-6))))
+        W = synth.weights(DECODE_TYPE, rows, K, [11, i])
+        t0 = time.perf_counter()
+        oracle.qlinear(DECODE_TYPE, W, rows, K, x, n_threads=cores)
+        total_s += time.perf_counter() - t0
+        total_bytes += alg_bytes(DECODE_TYPE, K, rows, DECODE_M)
+        rows_used.append(rows)
+    return {"value": round(total_bytes / total_s / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {rows_used} rows of the four (K,N) decode shapes, M=1, fp64, {total_s:.1f} s"}
+
+
+def run_reference(args):
+    """--impl reference: the oracle on the host cores, same metric and workload."""
+    cores = len(os.sched_getaffinity(0))
+    import oracle
+    oracle.build()
+    per_step = []
+    for s in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        cb = cpu_baseline(budget_s=args.cpu_budget / max(1, args.steps))
+        if s >= args.warmup:
+            per_step.append(cb["value"])
+    v = float(np.median(per_step))
+    return {"metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": "Q4_K decode, 8B-class layer: M=1, (K,N) in (4096,4096),(4096,1024),(4096,12288),(12288,4096)",
+                       "parallelism": "host cores"},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": cb["sample"]},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -9,11 +9,12 @@
 //   warps 0-7  dequantisers: warp w serves TMEM lane quarter w % 4 (rows 32(w%4)..+31, one
 //              thread per row) and half w / 4 of every 64-wide chunk. Each thread decodes its
 //              row's 32 weights of the chunk from the staged superblock into fp16 and writes
-//              them with tcgen05.st into a TMEM A-operand ring (4 chunks x 32 columns); the
+//              them with tcgen05.st into a TMEM A-operand ring (8 chunks x 32 columns); the
 //              MMA reads A straight from TMEM, so dequantised weights never touch shared
 //              memory. After the K loop the same warps drain the accumulator (tcgen05.ld) to y.
-//   warp 8     weight producer: bulk copies (TMA engine) of one superblock of the 128 rows
-//              into a shared-memory ring.
+//   warp 8     weight producer: one 2-D TMA tensor copy per stage (S superblocks of the 128
+//              rows) into a shared-memory ring when rows are 16-byte multiples, else one bulk
+//              copy per row over the aligned window around the row's span.
 //   warp 9     activation producer: 2-D TMA of the x tile [n_tile tokens x 64 k], 128-byte
 //              swizzled, the MMA's B operand.
 //   warp 10    TMEM allocator and the single MMA-issuing thread.
@@ -21,7 +22,6 @@
 // (status word set, TMEM freed).
 #include <cstdint>
 #include <cuda.h>
-#include <cudaTypedefs.h>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -32,7 +32,7 @@ namespace {
 
 constexpr int kRows = 128;          // weight rows per CTA (MMA M)
 constexpr int kChunkK = 64;         // k per pipeline chunk
-constexpr int kAStages = 4;         // TMEM A ring depth (chunks)
+constexpr int kAStages = 8;         // TMEM A ring depth (chunks): columns 256..511
 constexpr uint32_t kACol = 256;     // first TMEM column of the A ring
 constexpr int kDequantWarps = 8;
 constexpr int kThreads = 32 * 11;
@@ -44,7 +44,8 @@ struct GemmArgs {
     unsigned *status;
     int N, K, M, nsb;
     int n_tile;
-    uint32_t row_pitch;        // bytes per weight row in a quant stage
+    int S;                     // superblocks per weight stage
+    uint32_t row_pitch;        // bytes per weight row in a weight stage
     int qstages, bstages;
     uint32_t q_stage_bytes, b_stage_bytes;
     uint32_t q_off, bar_off;   // offsets from the 1024-aligned shared base
@@ -217,8 +218,9 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
 
 }  // namespace
 
-template <int TYPE>
-__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs p) {
+template <int TYPE, bool TMA>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap, const GemmArgs p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -266,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         tmem_relinquish();
     }
     if (warp == 9 && lane == 0) prefetch_tmap(&xmap);
+    if (TMA && warp == 8 && lane == 0) prefetch_tmap(&wmap);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -282,16 +285,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         uint32_t blk = 0;
         for (int chunk = 0; chunk < nchunks && ok; ++chunk) {
             const int sb = chunk >> 2, gg = chunk & 3;
-            const int qs = sb % QS;
+            const int si = sb / p.S, j = sb - si * p.S;   // weight stage and superblock within it
+            const int qs = si % QS;
             if (gg == 0) {
-                ok = wait_or_abort(qfull(qs), (sb / QS) & 1, abort_flag, p.status);
-                if (!ok) break;
-                const int64_t o = (static_cast<int64_t>(row) * p.nsb + sb) * p.bb;
-                blk = q_ring + qs * p.q_stage_bytes + r * p.row_pitch + static_cast<uint32_t>(o & 15);
+                if (j == 0) {
+                    ok = wait_or_abort(qfull(qs), (si / QS) & 1, abort_flag, p.status);
+                    ok = __all_sync(0xFFFFFFFFu, ok);
+                    if (!ok) break;
+                }
+                blk = q_ring + qs * p.q_stage_bytes + r * p.row_pitch + j * p.bb;
+                if constexpr (!TMA)   // block data starts (o & 15) bytes into the row's window
+                    blk += (static_cast<uint32_t>(row * p.nsb + si * p.S) * static_cast<uint32_t>(p.bb)) & 15u;
                 if constexpr (TYPE == 12 || TYPE == 13) kr = kq_row(blk, h);
             }
             const int sa = chunk % kAStages;
             ok = wait_or_abort(aempty(sa), ((chunk / kAStages) & 1) ^ 1, abort_flag, p.status);
+            ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
             tc_fence_after();
             uint32_t out[16];
@@ -305,11 +314,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(afull(sa));
-                if (gg == 3) mbar_arrive(qempty(qs));
+                if (gg == 3 && (j == p.S - 1 || sb == p.nsb - 1)) mbar_arrive(qempty(qs));
             }
         }
         // ---------------------------------------------------- epilogue: TMEM -> y
         if (ok) ok = wait_or_abort(accfull, 0, abort_flag, p.status);
+        ok = __all_sync(0xFFFFFFFFu, ok);
         if (ok) {
             tc_fence_after();
             const int half = p.n_tile / 2;
@@ -328,56 +338,65 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
     } else if (warp == 8) {
         // ---------------------------------------------------- weight producer
+        const int nstages = (p.nsb + p.S - 1) / p.S;
         int issued = 0;
-        for (int sb = 0; sb < p.nsb; ++sb) {
-            const int s = sb % QS;
-            if (!wait_or_abort(qempty(s), ((sb / QS) & 1) ^ 1, abort_flag, p.status)) break;
+        for (int si = 0; si < nstages; ++si) {
+            const int s = si % QS;
+            if (!wait_or_abort(qempty(s), ((si / QS) & 1) ^ 1, abort_flag, p.status)) break;
             fence_proxy_async_smem();
             const uint32_t st = q_ring + s * p.q_stage_bytes;
-            uint32_t my = 0;
-            const uint8_t *src[4];
-            uint32_t dst[4], nb[4];
-            int tail_len = 0;
-            uint32_t tail_dst = 0;
-            const uint8_t *tail_src = nullptr;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int rr = lane + 32 * i, rowi = n0 + rr;
-                nb[i] = 0;
-                src[i] = nullptr;
-                dst[i] = 0;
-                if (rowi < p.N) {
-                    const int64_t o = (static_cast<int64_t>(rowi) * p.nsb + sb) * p.bb;
-                    const int64_t lo = o & ~int64_t(15);
-                    int64_t hi = (o + p.bb + 15) & ~int64_t(15);
-                    const int64_t t16 = p.total_bytes & ~int64_t(15);
-                    if (hi > t16) {
-                        hi = t16;
-                        tail_len = static_cast<int>(o + p.bb - t16);
-                        tail_src = p.W + t16;
-                        tail_dst = st + rr * p.row_pitch + static_cast<uint32_t>(t16 - lo);
-                    }
-                    src[i] = p.W + lo;
-                    dst[i] = st + rr * p.row_pitch;
-                    nb[i] = static_cast<uint32_t>(hi - lo);
+            if constexpr (TMA) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(qfull(s), p.q_stage_bytes);
+                    tma_load_2d(st, &wmap, si * p.S * (p.bb / 4), n0, qfull(s));
                 }
-                my += nb[i];
-            }
-            if (tail_len > 0) {
-                uint8_t *gd = gbase + (tail_dst - base);
-                for (int i = 0; i < tail_len; ++i) gd[i] = __ldg(tail_src + i);
-            }
-            const uint32_t total = __reduce_add_sync(0xFFFFFFFFu, my);
-            __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(qfull(s), total);
-            __syncwarp();
+            } else {
+                const int sb = si * p.S, ns = min(p.S, p.nsb - sb);
+                uint32_t my = 0;
+                const uint8_t *src[4];
+                uint32_t dst[4], nb[4];
+                int tail_len = 0;
+                uint32_t tail_dst = 0;
+                const uint8_t *tail_src = nullptr;
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                if (nb[i]) bulk_g2s(dst[i], src[i], nb[i], qfull(s));
-            issued = sb + 1;
+                for (int i = 0; i < 4; ++i) {
+                    const int rr = lane + 32 * i, rowi = n0 + rr;
+                    nb[i] = 0;
+                    src[i] = nullptr;
+                    dst[i] = 0;
+                    if (rowi < p.N) {
+                        const int64_t o = (static_cast<int64_t>(rowi) * p.nsb + sb) * p.bb;
+                        const int64_t lo = o & ~int64_t(15);
+                        int64_t hi = (o + static_cast<int64_t>(ns) * p.bb + 15) & ~int64_t(15);
+                        const int64_t t16 = p.total_bytes & ~int64_t(15);
+                        if (hi > t16) {
+                            hi = t16;
+                            tail_len = static_cast<int>(o + static_cast<int64_t>(ns) * p.bb - t16);
+                            tail_src = p.W + t16;
+                            tail_dst = st + rr * p.row_pitch + static_cast<uint32_t>(t16 - lo);
+                        }
+                        src[i] = p.W + lo;
+                        dst[i] = st + rr * p.row_pitch;
+                        nb[i] = static_cast<uint32_t>(hi - lo);
+                    }
+                    my += nb[i];
+                }
+                if (tail_len > 0) {
+                    uint8_t *gd = gbase + (tail_dst - base);
+                    for (int i = 0; i < tail_len; ++i) gd[i] = __ldg(tail_src + i);
+                }
+                const uint32_t total = __reduce_add_sync(0xFFFFFFFFu, my);
+                __syncwarp();
+                if (lane == 0) mbar_arrive_expect_tx(qfull(s), total);
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (nb[i]) bulk_g2s(dst[i], src[i], nb[i], qfull(s));
+            }
+            issued = si + 1;
         }
         if (*abort_flag) {   // let issued copies land before the CTA's shared memory is released
-            for (int sb = max(0, issued - QS); sb < issued; ++sb) (void)mbar_wait(qfull(sb % QS), (sb / QS) & 1);
+            for (int si = max(0, issued - QS); si < issued; ++si) (void)mbar_wait(qfull(si % QS), (si / QS) & 1);
         }
     } else if (warp == 9) {
         // ---------------------------------------------------- activation producer
@@ -432,19 +451,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
 namespace {
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
 int pick_n_tile(int64_t M) {
     if (M >= 256) return 256;
     int n = static_cast<int>((M + 31) / 32) * 32;
@@ -452,17 +458,25 @@ int pick_n_tile(int64_t M) {
 }
 
 struct GemmPlan {
-    int n_tile, qstages, bstages;
+    int n_tile, qstages, bstages, S;
+    bool tma;
     uint32_t row_pitch, q_stage_bytes, b_stage_bytes, q_off, bar_off;
     size_t smem;
 };
 
-GemmPlan gemm_plan(int bb, int64_t M) {
+GemmPlan gemm_plan(int type, int bb, int64_t K, int64_t M) {
     GemmPlan pl{};
     pl.n_tile = pick_n_tile(M);
-    // window of one superblock incl. misalignment, rounded to an odd multiple of 16 bytes
-    uint32_t pitch = static_cast<uint32_t>((bb % 16 == 0) ? bb : ((bb + 30) & ~15));
-    if ((pitch / 16) % 2 == 0) pitch += 16;
+    const int64_t nsb = K / 256;
+    pl.S = (bb % 16 == 0) ? 1 : ((2 * bb) % 16 == 0 && nsb % 2 == 0) ? 2 : 1;
+    pl.tma = ((nsb * bb) % 16 == 0) && ((pl.S * bb) % 16 == 0) && type != 14;
+    uint32_t pitch;
+    if (pl.tma) {
+        pitch = static_cast<uint32_t>(pl.S * bb);   // dense rows as the tensor copy lands them
+    } else {   // window of the span incl. misalignment, an odd multiple of 16 bytes
+        pitch = static_cast<uint32_t>((pl.S * bb + 30) & ~15);
+        if ((pitch / 16) % 2 == 0) pitch += 16;
+    }
     pl.row_pitch = pitch;
     pl.q_stage_bytes = kRows * pitch;
     pl.b_stage_bytes = static_cast<uint32_t>(pl.n_tile) * 128u;
@@ -470,7 +484,7 @@ GemmPlan gemm_plan(int bb, int64_t M) {
     for (int bs = 4; bs >= 2; --bs) {
         for (int qs = 3; qs >= 2; --qs) {
             const size_t q_off = static_cast<size_t>(bs) * pl.b_stage_bytes;
-            const size_t bar_off = q_off + static_cast<size_t>(qs) * pl.q_stage_bytes;
+            const size_t bar_off = (q_off + static_cast<size_t>(qs) * pl.q_stage_bytes + 15) & ~size_t(15);
             const size_t total = bar_off + 8 * (2 * qs + 2 * bs + 2 * kAStages + 1) + 16;
             if (total <= limit) {
                 pl.bstages = bs;
@@ -486,18 +500,27 @@ GemmPlan gemm_plan(int bb, int64_t M) {
     return pl;
 }
 
-template <int TYPE>
-cudaError_t launch_t(const CUtensorMap &xmap, const GemmArgs &a, dim3 grid, size_t smem, cudaStream_t st) {
+template <int TYPE, bool TMA>
+cudaError_t launch_t(const CUtensorMap &xmap, const CUtensorMap &wmap, const GemmArgs &a, dim3 grid, size_t smem,
+                     cudaStream_t st) {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<TYPE>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        cudaError_t e =
+            cudaFuncSetAttribute(gemm_kernel<TYPE, TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    gemm_kernel<TYPE><<<grid, kThreads, smem, st>>>(xmap, a);
+    gemm_kernel<TYPE, TMA><<<grid, kThreads, smem, st>>>(xmap, wmap, a);
     return cudaGetLastError();
+}
+
+template <int TYPE>
+cudaError_t launch_type(bool tma, const CUtensorMap &xmap, const CUtensorMap &wmap, const GemmArgs &a, dim3 grid,
+                        size_t smem, cudaStream_t st) {
+    return tma ? launch_t<TYPE, true>(xmap, wmap, a, grid, smem, st)
+               : launch_t<TYPE, false>(xmap, wmap, a, grid, smem, st);
 }
 
 }  // namespace
@@ -506,22 +529,20 @@ int gemm_launch_count(int, int64_t, int64_t, int64_t) { return 1; }
 
 cudaError_t gemm_launch(int type, const uint8_t *W, const __half *x, float *y, int64_t N, int64_t K, int64_t M,
                         unsigned *status, int, cudaStream_t stream) {
-    const int bb = gemv_block_bytes(type);
+    const int bb = block_bytes_of(type);
     if (bb < 0) return cudaErrorInvalidValue;
-    const GemmPlan pl = gemm_plan(bb, M);
+    const GemmPlan pl = gemm_plan(type, bb, K, M);
     if (pl.n_tile == 0) return cudaErrorNotSupported;
-    auto enc = encode_fn();
-    if (!enc) return cudaErrorNotSupported;
-
-    CUtensorMap xmap;
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
-    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(K) * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kChunkK), static_cast<cuuint32_t>(pl.n_tile)};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult cr = enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half *>(x), gdim, gstride, box, estr,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    CUtensorMap xmap{}, wmap{};
+    if (!encode_tmap_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
+                        static_cast<uint64_t>(K) * 2, kChunkK, static_cast<uint32_t>(pl.n_tile), true))
+        return cudaErrorNotSupported;
+    if (pl.tma) {
+        const uint64_t row_words = static_cast<uint64_t>(K / 256) * bb / 4;
+        if (!encode_tmap_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, W, row_words, static_cast<uint64_t>(N), row_words * 4,
+                            static_cast<uint32_t>(pl.S * bb / 4), kRows, false))
+            return cudaErrorNotSupported;
+    }
 
     GemmArgs a{};
     a.W = W;
@@ -532,6 +553,7 @@ cudaError_t gemm_launch(int type, const uint8_t *W, const __half *x, float *y, i
     a.M = static_cast<int>(M);
     a.nsb = static_cast<int>(K / 256);
     a.n_tile = pl.n_tile;
+    a.S = pl.S;
     a.row_pitch = pl.row_pitch;
     a.qstages = pl.qstages;
     a.bstages = pl.bstages;
@@ -544,10 +566,10 @@ cudaError_t gemm_launch(int type, const uint8_t *W, const __half *x, float *y, i
     a.type = type;
     const dim3 grid(static_cast<unsigned>((N + kRows - 1) / kRows), static_cast<unsigned>((M + pl.n_tile - 1) / pl.n_tile));
     switch (type) {
-    case 12: return launch_t<12>(xmap, a, grid, pl.smem, stream);
-    case 13: return launch_t<13>(xmap, a, grid, pl.smem, stream);
-    case 14: return launch_t<14>(xmap, a, grid, pl.smem, stream);
-    case 23: return launch_t<23>(xmap, a, grid, pl.smem, stream);
+    case 12: return launch_type<12>(pl.tma, xmap, wmap, a, grid, pl.smem, stream);
+    case 13: return launch_type<13>(pl.tma, xmap, wmap, a, grid, pl.smem, stream);
+    case 14: return launch_type<14>(pl.tma, xmap, wmap, a, grid, pl.smem, stream);
+    case 23: return launch_type<23>(pl.tma, xmap, wmap, a, grid, pl.smem, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -3,27 +3,37 @@
 // Design (sm_103a):
 //  * One CTA per 16 weight rows (one MMA row tile). Its warps split K: warp w owns a
 //    contiguous range of superblocks and streams them through its own ring of shared-memory
-//    stages. Each stage holds one superblock of all 16 rows plus the matching 256 columns of
-//    x for every token; it is filled by bulk copies (the TMA engine, cp.async.bulk) that
-//    complete on the stage's mbarrier, so HBM bytes in flight cost no registers.
-//  * Every weight byte is read from HBM exactly once. Each lane decodes its share of the
-//    block in registers into fp16 pairs that are EXACT small integers (sc*q for K-quants,
-//    sc*(q-32) for Q6_K, (ls-32)*codebook[q] for IQ4_XS), feeds them to the legacy tensor
-//    core (mma.sync m16n8k16, fp32 accumulate) with the tokens on the MMA's n = 8 side, and
-//    applies the fp32 superblock scale d (and dmin for K-quants) to the per-superblock
-//    fp32 partial sums. The K-quant min term dmin * sum_j m_j * sum(x over sub-block j) runs
-//    through a second MMA whose A operand is the (constant per sub-block) 6-bit min.
-//  * Warps' partial tiles are reduced in fixed order through shared memory (deterministic,
-//    no atomics).
+//    stages. A stage holds S superblocks of all 16 rows and is filled by ONE 2-D TMA tensor
+//    copy (rows whose byte length is a multiple of 16), else by one bulk copy per row over
+//    the 16-byte aligned window around the row's span. Copies complete on the stage's
+//    mbarrier, so HBM bytes in flight cost no registers, and every weight byte is read from
+//    HBM exactly once.
+//  * x for the warp's K range is staged once into shared memory through registers, in the
+//    order the MMA fragments want (see below), with 16 bytes of padding per 64 columns.
+//  * Each lane decodes its share of a block in registers into fp16 pairs that are EXACT
+//    integers (sc*q for K-quants, sc*(q-32) for Q6_K, (ls-32)*codebook[q] for IQ4_XS,
+//    the last two rounded only beyond 2048) and feeds them to the legacy tensor core
+//    (mma.sync m16n8k16, fp32 accumulate) with the tokens on the MMA's n = 8 side. The fp32
+//    superblock scale d (and dmin) is applied to per-superblock fp32 partial sums; the K-quant
+//    min term dmin * sum_j m_j * sum(x over sub-block j) runs through a second MMA whose A
+//    operand is the 6-bit min, constant per sub-block.
+//  * Warps' partial tiles are reduced in fixed order through shared memory (deterministic).
 // MMA fragment ownership (m16n8k16): lane = 4*g + c holds rows g and g+8 of A and k-slots
 // {2c, 2c+1, 2c+8, 2c+9}. The contraction does not care which real k sits in which slot, so
-// each lane assigns the k's it decoded to its own slots and loads x for exactly those k's.
+// each lane assigns the k's it decoded to its own slots and reads x for exactly those k's.
+// A 32-bit word of packed quants holds bytes b0..b3 of consecutive positions; masking it
+// directly yields the half pairs (b0, b2) and (b1, b3), so x is staged with each group of
+// four columns stored as [x0 x2 x1 x3] and one 8-byte read gives both B registers.
+#include <algorithm>
 #include <cstdint>
+#include <cuda.h>
 
 #include "kernels.h"
 #include "ptx.cuh"
 
 namespace ql {
+
+namespace {
 
 template <int TYPE>
 struct GemvFmt;
@@ -44,11 +54,25 @@ struct GemvFmt<23> {   // IQ4_XS
     static constexpr int BB = 136;
 };
 
-// x segment layout inside a stage: token t, 64-column segment s at t*kXTok + s*kXSeg.
-// 16 bytes of padding per 128-byte segment spread the four lanes of a row group (which read
-// segments c = 0..3) over distinct banks.
-constexpr uint32_t kXSeg = 144;
-constexpr uint32_t kXTok = 4 * kXSeg;
+struct GemvArgs {
+    const uint8_t *W;
+    const __half *x;
+    float *y;
+    unsigned *status;
+    int N, K, M, nsb;
+    int S;                   // superblocks per stage
+    int kw;                  // superblocks of the K slice each warp owns
+    int stages;              // ring depth per warp
+    int xres;                // 1: x slice resident per warp; 0: x travels with each stage
+    uint32_t row_pitch;      // bytes between rows inside a stage
+    uint32_t w_bytes;        // weight bytes of a stage (16 * row_pitch)
+    uint32_t x_bytes;        // per-stage x bytes inside a ring slot (0 when resident)
+    uint32_t x_tx;           // bytes one x tensor copy delivers (all tokens)
+    uint32_t x_warp_bytes;   // resident x region per warp
+    uint32_t slot_bytes;     // one ring slot, rounded to 1 KB
+    uint32_t red_offset, x_offset, ring_offset;
+    int64_t total_bytes;     // bytes of W
+};
 
 // ---------------------------------------------------------------- K-quant scale constants
 
@@ -81,21 +105,20 @@ __device__ __forceinline__ KqConsts kq_consts(uint4 h, int c) {
 }
 
 // One qs word of a K-quant row -> the four A pairs (exact sc*q in fp16).
-// w holds qs bytes [b0 b1 b2 b3] = positions l..l+3 of a 32-byte group: low nibbles are
-// weights l..l+3 of sub-block 2c, high nibbles weights l..l+3 of sub-block 2c+1.
-// qh (Q5_K only) holds qh[l..l+3]; bit 2c / 2c+1 of each byte is the fifth bit.
+// w = qs bytes [b0 b1 b2 b3] at positions l..l+3 of 32-byte group c: low nibbles are weights
+// of sub-block 2c, high nibbles of sub-block 2c+1. Reordered to [b0 b2 b1 b3] so that each
+// half lane holds neighbouring positions: pairs (b0, b1) and (b2, b3), i.e. columns (k, k+1).
+// qh (Q5_K only) = qh[l..l+3]; bit 2c / 2c+1 of each byte is the fifth bit.
 template <bool Q5>
 __device__ __forceinline__ void kq_word(uint32_t w, uint32_t qh, int c, const KqConsts &k, uint32_t &lo01,
                                         uint32_t &lo23, uint32_t &hi01, uint32_t &hi23) {
-    const uint32_t w2 = prmt(w, 0u, 0x3120u);   // [b0 b2 b1 b3]: half lanes hold b0|b1, then b2|b3
-    const uint32_t w3 = w2 >> 8;
+    const uint32_t w2 = prmt(w, 0u, 0x3120u), w3 = w2 >> 8;
     uint32_t l01 = and_or(w2, 0x000F000Fu, kH2_1024);   // (1024 + q)
     uint32_t l23 = and_or(w3, 0x000F000Fu, kH2_1024);
     uint32_t h01 = and_or(w2, 0x00F000F0u, kH2_1024);   // (1024 + 16 q)
     uint32_t h23 = and_or(w3, 0x00F000F0u, kH2_1024);
     if constexpr (Q5) {
-        const uint32_t q2 = prmt(qh, 0u, 0x3120u);
-        const uint32_t q3 = q2 >> 8;
+        const uint32_t q2 = prmt(qh, 0u, 0x3120u), q3 = q2 >> 8;
         const uint32_t rl = (4u - 2u * c) & 31u, rh = (7u - 2u * c) & 31u;
         l01 = or_and(l01, rotl(q2, rl), 0x00100010u);   // bit 2c   -> bit 4 (+16)
         l23 = or_and(l23, rotl(q3, rl), 0x00100010u);
@@ -124,16 +147,24 @@ __device__ __forceinline__ uint32_t word4(const uint4 &a, int u) {
     return u == 0 ? a.x : u == 1 ? a.y : u == 2 ? a.z : a.w;
 }
 
+// x of one stage: token t, 64-column segment R (= 4 * superblock + segment) is the 128-byte
+// row t * 4S + R of a tile the TMA wrote with the 128-byte swizzle (16-byte chunk p of row r
+// stored at chunk p ^ (r & 7)). xrow(r) gives the row base, chunk address = base ^ key.
+struct XRow {
+    uint32_t base, key;
+};
+__device__ __forceinline__ XRow xrow(uint32_t xst, uint32_t r) { return XRow{xst + r * 128u, (r & 7u) << 4}; }
+__device__ __forceinline__ uint4 ldx(const XRow &x, uint32_t p) { return lds128(x.base + ((p << 4) ^ x.key)); }
+
 // ---------------------------------------------------------------- per-format superblock
 
-// Q4_K / Q5_K: lane (g, c) decodes the 32-byte qs group c (64 weights: sub-blocks 2c, 2c+1)
-// of rows g and g+8.
+// Q4_K / Q5_K: lane (g, c) decodes 32-byte qs group c (sub-blocks 2c, 2c+1) of rows g, g+8.
+// xr = row of columns 64c .. 64c+63 of this superblock.
 template <int TYPE>
-__device__ __forceinline__ void superblock_kq(uint32_t blk_a, uint32_t blk_b, uint32_t xb, int c, float (&acc)[4]) {
+__device__ __forceinline__ void superblock_kq(uint32_t blk_a, uint32_t blk_b, const XRow &xr, int c, float (&acc)[4]) {
     constexpr bool Q5 = (TYPE == 13);
     constexpr uint32_t QS = Q5 ? 48 : 16;
     const uint4 ha = lds128(blk_a), hb = lds128(blk_b);
-    const KqConsts ka = kq_consts(ha, c), kb = kq_consts(hb, c);
     const uint4 qa0 = lds128(blk_a + QS + 32 * c), qa1 = lds128(blk_a + QS + 32 * c + 16);
     const uint4 qb0 = lds128(blk_b + QS + 32 * c), qb1 = lds128(blk_b + QS + 32 * c + 16);
     uint4 ha0 = make_uint4(0, 0, 0, 0), ha1 = ha0, hb0 = ha0, hb1 = ha0;
@@ -143,22 +174,22 @@ __device__ __forceinline__ void superblock_kq(uint32_t blk_a, uint32_t blk_b, ui
         hb0 = lds128(blk_b + 16);
         hb1 = lds128(blk_b + 32);
     }
+    const KqConsts ka = kq_consts(ha, c), kb = kq_consts(hb, c);
     float d1[4] = {0.f, 0.f, 0.f, 0.f}, d2[4] = {0.f, 0.f, 0.f, 0.f};
-    const uint32_t xs = xb + c * kXSeg;   // segment c holds columns 64c .. 64c+63
 #pragma unroll
     for (int u = 0; u < 8; u += 2) {
-        const uint4 xl = lds128(xs + 8 * u);        // columns 64c + 4u .. +7   (low nibbles)
-        const uint4 xh = lds128(xs + 64 + 8 * u);   // columns 64c + 32 + 4u .. (high nibbles)
+        const uint4 xl = ldx(xr, u >> 1);         // columns 64c + 4u .. +7   (low nibbles)
+        const uint4 xh = ldx(xr, 4 + (u >> 1));   // columns 64c + 32 + 4u .. (high nibbles)
 #pragma unroll
         for (int v = 0; v < 2; ++v) {
             const int uu = u + v;
-            uint32_t la01, la23, lh01, lh23, lb01, lb23, lbh01, lbh23;
-            kq_word<Q5>(word_of(qa0, qa1, uu), word_of(ha0, ha1, uu), c, ka, la01, la23, lh01, lh23);
-            kq_word<Q5>(word_of(qb0, qb1, uu), word_of(hb0, hb1, uu), c, kb, lb01, lb23, lbh01, lbh23);
+            uint32_t la01, la23, ha01, ha23, lb01, lb23, hb01, hb23;
+            kq_word<Q5>(word_of(qa0, qa1, uu), word_of(ha0, ha1, uu), c, ka, la01, la23, ha01, ha23);
+            kq_word<Q5>(word_of(qb0, qb1, uu), word_of(hb0, hb1, uu), c, kb, lb01, lb23, hb01, hb23);
             const uint32_t x0 = v ? xl.z : xl.x, x1 = v ? xl.w : xl.y;
             const uint32_t y0 = v ? xh.z : xh.x, y1 = v ? xh.w : xh.y;
             mma16816(d1, la01, lb01, la23, lb23, x0, x1);
-            mma16816(d1, lh01, lbh01, lh23, lbh23, y0, y1);
+            mma16816(d1, ha01, hb01, ha23, hb23, y0, y1);
             mma16816(d2, ka.m_lo, kb.m_lo, ka.m_lo, kb.m_lo, x0, x1);
             mma16816(d2, ka.m_hi, kb.m_hi, ka.m_hi, kb.m_hi, y0, y1);
         }
@@ -189,43 +220,36 @@ __device__ __forceinline__ uint2 lds64_a2(uint32_t addr) {
 // all four quarters t (64 weights per row): ql bytes 64h+16e.. (t = 0 low / t = 2 high
 // nibbles), 64h+32+16e.. (t = 1 / t = 3), qh bytes 128+32h+16e.. (bits 2t, 2t+1).
 __device__ __forceinline__ void q6_row_consts(uint32_t blk, int h, int e, uint32_t (&sc)[4], float &d) {
-    const uint2 s = lds64_a2(blk + 192 + 8 * h);        // int8 scales 8h .. 8h+7
+    const uint2 s = lds64_a2(blk + 192 + 8 * h);                       // int8 scales 8h .. 8h+7
     const uint32_t s0 = s.x ^ 0x80808080u, s1 = s.y ^ 0x80808080u;   // sc + 128 as unsigned bytes
-    // lane needs scales 8h + e + 2t: bytes e, e+2 of s0 (t = 0, 1) and of s1 (t = 2, 3)
     const uint32_t sel0 = e ? 0x4141u : 0x4040u, sel1 = e ? 0x4343u : 0x4242u;
     const uint32_t kH2_1152 = 0x64806480u;
-    sc[0] = hsub2(prmt(s0, 0x64646464u, sel0), kH2_1152);
+    sc[0] = hsub2(prmt(s0, 0x64646464u, sel0), kH2_1152);   // scale 8h + e + 2t
     sc[1] = hsub2(prmt(s0, 0x64646464u, sel1), kH2_1152);
     sc[2] = hsub2(prmt(s1, 0x64646464u, sel0), kH2_1152);
     sc[3] = hsub2(prmt(s1, 0x64646464u, sel1), kH2_1152);
     d = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(blk + 208))));
 }
 
-// A pairs of quarter t for one word triple (ql word for t%2, qh word); returns (k0,k0+1)
-// and (k0+2,k0+3) as exact sc*(q-32).
+// A pairs of quarter t for one (ql word, qh word): columns (k0, k0+1), (k0+2, k0+3) as sc*(q-32).
 __device__ __forceinline__ void q6_pairs(uint32_t qlw, uint32_t qhw, int t, uint32_t sc, uint32_t &p01, uint32_t &p23) {
-    const uint32_t l2 = prmt(qlw, 0u, 0x3120u);
+    uint32_t l2 = prmt(qlw, 0u, 0x3120u);
+    if (t >= 2) l2 >>= 4;
     const uint32_t h2 = prmt(qhw, 0u, 0x3120u);
-    const uint32_t l3 = l2 >> 8, h3 = h2 >> 8;
-    uint32_t v01, v23;
-    if (t < 2) {
-        v01 = and_or(l2, 0x000F000Fu, kH2_1024);
-        v23 = and_or(l3, 0x000F000Fu, kH2_1024);
-    } else {
-        v01 = and_or(l2 >> 4, 0x000F000Fu, kH2_1024);
-        v23 = and_or(l3 >> 4, 0x000F000Fu, kH2_1024);
-    }
+    uint32_t v01 = and_or(l2, 0x000F000Fu, kH2_1024);
+    uint32_t v23 = and_or(l2 >> 8, 0x000F000Fu, kH2_1024);
     // bits 2t, 2t+1 of each qh byte -> bits 4, 5 of the half
     const int sh = 4 - 2 * t;
-    const uint32_t b01 = sh >= 0 ? (h2 << sh) : (h2 >> -sh);
-    const uint32_t b23 = sh >= 0 ? (h3 << sh) : (h3 >> -sh);
-    v01 = or_and(v01, b01, 0x00300030u);
-    v23 = or_and(v23, b23, 0x00300030u);
+    const uint32_t h3 = h2 >> 8;
+    v01 = or_and(v01, sh >= 0 ? (h2 << sh) : (h2 >> -sh), 0x00300030u);
+    v23 = or_and(v23, sh >= 0 ? (h3 << sh) : (h3 >> -sh), 0x00300030u);
     p01 = hmul2(hsub2(v01, kH2_1056), sc);   // (q - 32) * sc
     p23 = hmul2(hsub2(v23, kH2_1056), sc);
 }
 
-__device__ __forceinline__ void superblock_q6(uint32_t blk_a, uint32_t blk_b, uint32_t xb, int c, float (&acc)[4]) {
+// xs = x tile of this stage, r0 = token row base (tok * 4S + 4j).
+__device__ __forceinline__ void superblock_q6(uint32_t blk_a, uint32_t blk_b, uint32_t xs, uint32_t r0, int c,
+                                              float (&acc)[4]) {
     const int h = c >> 1, e = c & 1;
     uint32_t sca[4], scb[4];
     float da, db;
@@ -237,11 +261,11 @@ __device__ __forceinline__ void superblock_q6(uint32_t blk_a, uint32_t blk_b, ui
     float d1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-        // columns 128h + 32t + 16e + 4u: segment 2h + t/2, offset 32(t%2) + 16e + 4u
-        const uint32_t xs = xb + (2 * h + t / 2) * kXSeg + 2 * (32 * (t & 1) + 16 * e);
+        // columns 128h + 32t + 16e + 4u: segment 2h + t/2, chunk 4(t%2) + 2e + u/2
+        const XRow xr = xrow(xs, r0 + 2 * h + t / 2);
 #pragma unroll
         for (int u = 0; u < 4; u += 2) {
-            const uint4 xv = lds128(xs + 8 * u);
+            const uint4 xv = ldx(xr, 4 * (t & 1) + 2 * e + (u >> 1));
 #pragma unroll
             for (int v = 0; v < 2; ++v) {
                 const int uu = u + v;
@@ -259,11 +283,11 @@ __device__ __forceinline__ void superblock_q6(uint32_t blk_a, uint32_t blk_b, ui
 }
 
 // IQ4_XS codebook (test/unit/test_llm_quant_cpu.py, test_unpack_lut_dot_uop) stored as
-// unsigned bytes value + 128, four entries per register.
-constexpr uint32_t kIq4T0 = 0x3F2D1801u;   //  -65  -83 -104 -127
-constexpr uint32_t kIq4T1 = 0x766A5D4Fu;   //  -10  -22  -35  -49
-constexpr uint32_t kIq4T2 = 0xA6998D81u;   //   38   25   13    1
-constexpr uint32_t kIq4T3 = 0xF1D9C5B5u;   //  113   89   69   53
+// unsigned bytes value + 128, four entries per register, entry 0 in the low byte.
+constexpr uint32_t kIq4T0 = 0x3F2D1801u;   // -127 -104  -83  -65
+constexpr uint32_t kIq4T1 = 0x766A5D4Fu;   //  -49  -35  -22  -10
+constexpr uint32_t kIq4T2 = 0xA6998D81u;   //    1   13   25   38
+constexpr uint32_t kIq4T3 = 0xF1D9C5B5u;   //   53   69   89  113
 
 // Codebook lookup of the four nibbles of the low 16 bits of `s` (in nibble order) ->
 // four bytes (value + 128).
@@ -301,13 +325,12 @@ __device__ __forceinline__ void iq4_word(uint32_t w, uint32_t ls, uint32_t nb, u
     hi23 = hfma2(prmt(r23, 0x64646464u, 0x4341u), ls, nb);
 }
 
-__device__ __forceinline__ void superblock_iq4(uint32_t blk_a, uint32_t blk_b, uint32_t xb, int c, float (&acc)[4]) {
+__device__ __forceinline__ void superblock_iq4(uint32_t blk_a, uint32_t blk_b, const XRow &xr, int c, float (&acc)[4]) {
     uint32_t lsa[2], nba[2], lsb[2], nbb[2];
     float da, db;
     iq4_row_consts(blk_a, c, lsa, nba, da);
     iq4_row_consts(blk_b, c, lsb, nbb, db);
     float d1[4] = {0.f, 0.f, 0.f, 0.f};
-    const uint32_t xs = xb + c * kXSeg;   // sub-blocks 2c, 2c+1 = columns 64c .. 64c+63
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
         const uint32_t qoff = 8 + 32 * c + 16 * j;
@@ -315,8 +338,8 @@ __device__ __forceinline__ void superblock_iq4(uint32_t blk_a, uint32_t blk_b, u
         const uint2 b0 = lds64(blk_b + qoff), b1 = lds64(blk_b + qoff + 8);
 #pragma unroll
         for (int u = 0; u < 4; u += 2) {
-            const uint4 xl = lds128(xs + 2 * (32 * j + 4 * u));        // columns 32j + 4u ..
-            const uint4 xh = lds128(xs + 2 * (32 * j + 16 + 4 * u));   // columns 32j + 16 + 4u ..
+            const uint4 xl = ldx(xr, 4 * j + (u >> 1));       // columns 64c + 32j + 4u ..
+            const uint4 xh = ldx(xr, 4 * j + 2 + (u >> 1));   // columns 64c + 32j + 16 + 4u ..
 #pragma unroll
             for (int v = 0; v < 2; ++v) {
                 const int uu = u + v;
@@ -337,230 +360,301 @@ __device__ __forceinline__ void superblock_iq4(uint32_t blk_a, uint32_t blk_b, u
 }
 
 // ---------------------------------------------------------------- the kernel
+//
+// Persistent: CTA b owns a contiguous run of 16-row tiles (an equal share of the T = N/16
+// tiles, G = grid size, one CTA per SM) and walks them in order; warp w owns the
+// fixed K slice of superblocks [w kw, (w+1) kw) for every tile, so its slice of x is loaded
+// once (xres) or, when that does not fit, with each stage. Each warp streams its units
+// (tile, stage of S superblocks) through a ring of `stages` slots, issuing a slot's next
+// unit as soon as it has consumed it, across tile boundaries. After each tile the warps'
+// 16 x 8 partial tiles are summed in fixed order through shared memory.
 
-template <int TYPE>
-__global__ void __launch_bounds__(512) gemv_kernel(const GemvArgs p) {
+template <int TYPE, bool TMA>
+__global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                      const __grid_constant__ CUtensorMap xmap, const GemvArgs p) {
     constexpr int BB = GemvFmt<TYPE>::BB;
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem[];
     const int nwarps = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
-    const int row0 = blockIdx.x * 16;
-    const int D = p.stages;
+    const int D = p.stages, S = p.S;
 
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);               // [nwarps][D]
-    float *red = reinterpret_cast<float *>(smem + p.red_offset);       // [nwarps][32][4]
-    const uint32_t region = smem_u32(smem + p.region_offset) + warp * p.warp_bytes;
-    const uint32_t bar0 = smem_u32(bars + warp * D);
+    const uint32_t base = (smem_u32(smem) + 1023u) & ~1023u;   // the launch adds 1 KB of slack
+    uint8_t *const gbase = smem + (base - smem_u32(smem));
+    float *red = reinterpret_cast<float *>(gbase + p.red_offset);   // [2][nwarps][32][4]
+    const uint32_t bar0 = base + 8u * warp * (D + 1);              // D ring barriers + 1 x barrier
+    const uint32_t xbar = bar0 + 8u * D;
+    const uint32_t xreg = base + p.x_offset + warp * p.x_warp_bytes;
+    const uint32_t ring = base + p.ring_offset + warp * D * p.slot_bytes;
 
-    const int sb_begin = warp * p.sb_per_warp;
-    const int sb_end = min(sb_begin + p.sb_per_warp, p.nsb);
-    const int nmine = max(sb_end - sb_begin, 0);
+    const int G = gridDim.x, b = blockIdx.x;
+    const int T = (p.N + 15) / 16;   // row tiles; CTA b owns tiles [T b / G, T (b+1) / G)
+    const int t_begin = static_cast<int>(static_cast<int64_t>(T) * b / G);
+    const int t_end = static_cast<int>(static_cast<int64_t>(T) * (b + 1) / G);
+    const int r_begin = 16 * t_begin, r_end = min(p.N, 16 * t_end);
+    const int ntiles = t_end - t_begin;
+
+    const int kb0 = warp * p.kw;
+    const int kb1 = min(kb0 + p.kw, p.nsb);
+    const int nmine = max(kb1 - kb0, 0);
+    const int nst = (nmine + S - 1) / S;   // stages per tile for this warp (0 for idle warps)
+    const int total = ntiles * nst;
 
     if (lane == 0) {
-        for (int s = 0; s < D; ++s) mbar_init(bar0 + 8 * s, 1);
+        for (int s = 0; s <= D; ++s) mbar_init(bar0 + 8 * s, 1);
         fence_mbar_init();
+        prefetch_tmap(&xmap);
+        if constexpr (TMA) prefetch_tmap(&wmap);
     }
     __syncwarp();
 
-    const int64_t nsb = p.nsb;
-    const int ncopy = 16 + 4 * p.M;
+    // x slot of a ring slot (per-stage x) sits in front of its weights
+    auto wslot = [&](int s) { return ring + s * p.slot_bytes + (p.xres ? 0u : p.x_bytes); };
+    auto xslot = [&](int s) { return ring + s * p.slot_bytes; };
 
-    // Fill stage buffer `s` with superblock `sb` of rows row0..row0+15 and x columns
-    // 256 sb .. 256 sb + 255 of every token.
-    auto issue = [&](int s, int sb) {
-        const uint32_t st = region + s * p.stage_bytes;
+    auto issue = [&](int s, int u) {
+        const int t = u / nst, si = u - t * nst;
+        const int sb = kb0 + si * S;
+        const int row0 = r_begin + 16 * t;
         const uint32_t bar = bar0 + 8 * s;
-        uint32_t my_bytes = 0;
-        const uint8_t *src[2];
-        uint32_t dst[2], nbytes[2];
-        int tail_len = 0;
-        uint32_t tail_dst = 0;
-        const uint8_t *tail_src = nullptr;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int q = lane + 32 * r;
-            nbytes[r] = 0;
-            src[r] = nullptr;
-            dst[r] = 0;
-            if (q < 16) {
-                const int row = row0 + q;
-                if (row < p.N) {
-                    const int64_t o = (static_cast<int64_t>(row) * nsb + sb) * BB;
-                    const int64_t lo = o & ~int64_t(15);
-                    int64_t hi = (o + BB + 15) & ~int64_t(15);
-                    const int64_t t16 = p.total_bytes & ~int64_t(15);
-                    if (hi > t16) {   // last block of a buffer whose size is not a multiple of 16
-                        hi = t16;
-                        tail_len = static_cast<int>(o + BB - t16);
-                        tail_src = p.W + t16;
-                        tail_dst = st + q * p.row_pitch + static_cast<uint32_t>(t16 - lo);
-                    }
-                    src[r] = p.W + lo;
-                    dst[r] = st + q * p.row_pitch;
-                    nbytes[r] = static_cast<uint32_t>(hi - lo);
-                }
-            } else if (q < ncopy) {
-                const int t = (q - 16) >> 2, seg = (q - 16) & 3;
-                src[r] = reinterpret_cast<const uint8_t *>(p.x + static_cast<int64_t>(t) * p.K + sb * 256 + seg * 64);
-                dst[r] = st + 16 * p.row_pitch + t * kXTok + seg * kXSeg;
-                nbytes[r] = 128;
+        const uint32_t xtx = p.xres ? 0u : p.x_tx;
+        if constexpr (TMA) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar, p.w_bytes + xtx);
+                tma_load_2d(wslot(s), &wmap, sb * (BB / 8), row0, bar);
+                if (!p.xres) tma_load_3d(xslot(s), &xmap, 0, sb * 4, 0, bar);
             }
-            my_bytes += nbytes[r];
-        }
-        const uint32_t total = __reduce_add_sync(0xFFFFFFFFu, my_bytes);
-        if (lane == 0) mbar_arrive_expect_tx(bar, total);
-        __syncwarp();
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-            if (nbytes[r]) bulk_g2s(dst[r], src[r], nbytes[r], bar);
-        if (tail_len > 0) {
-            uint8_t *gdst = reinterpret_cast<uint8_t *>(smem) + (tail_dst - smem_u32(smem));
-            for (int i = 0; i < tail_len; ++i) gdst[i] = __ldg(tail_src + i);
+        } else {
+            const int ns = min(S, kb1 - sb);
+            uint32_t nbytes = 0, dst = 0;
+            const uint8_t *src = nullptr;
+            int tail_len = 0;
+            uint32_t tail_off = 0;
+            int64_t t16 = 0;
+            if (lane < 16 && row0 + lane < r_end) {
+                const int64_t o = (static_cast<int64_t>(row0 + lane) * p.nsb + sb) * BB;
+                const int64_t lo = o & ~int64_t(15);
+                int64_t hi = (o + static_cast<int64_t>(ns) * BB + 15) & ~int64_t(15);
+                t16 = p.total_bytes & ~int64_t(15);
+                if (hi > t16) {   // the span ends in the last, partial 16 bytes of W
+                    hi = t16;
+                    tail_len = static_cast<int>(o + static_cast<int64_t>(ns) * BB - t16);
+                    tail_off = static_cast<uint32_t>(t16 - lo);
+                }
+                src = p.W + lo;
+                dst = wslot(s) + lane * p.row_pitch;
+                nbytes = static_cast<uint32_t>(hi - lo);
+            }
+            if (tail_len > 0) {
+                uint8_t *gd = smem + (dst + tail_off - smem_u32(smem));
+                for (int i = 0; i < tail_len; ++i) gd[i] = __ldg(p.W + t16 + i);
+            }
+            const uint32_t sum = __reduce_add_sync(0xFFFFFFFFu, nbytes);
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar, sum + xtx);
+                if (!p.xres) tma_load_3d(xslot(s), &xmap, 0, sb * 4, 0, bar);
+            }
+            __syncwarp();
+            if (nbytes) bulk_g2s(dst, src, nbytes, bar);
         }
     };
 
-    for (int s = 0; s < D && s < nmine; ++s) issue(s, sb_begin + s);
-
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
     bool ok = true;
-    int it = 0;
-    const int tok = min(g, p.M - 1);
-    for (; it < nmine; ++it) {
-        const int s = it % D;
-        const uint32_t parity = (it / D) & 1;
-        if (!mbar_wait(bar0 + 8 * s, parity)) {
-            ok = false;
-            break;
-        }
-        const int sb = sb_begin + it;
-        const uint32_t st = region + s * p.stage_bytes;
+    if (p.xres && nmine > 0 && lane == 0) {   // this warp's x slice, all tokens, once
+        mbar_arrive_expect_tx(xbar, p.x_tx);
+        tma_load_3d(xreg, &xmap, 0, kb0 * 4, 0, xbar);
+    }
+    for (int s = 0; s < D && s < total; ++s) issue(s, s);
+    if (p.xres && nmine > 0) ok = mbar_wait(xbar, 0);
+
+    const uint32_t tok = static_cast<uint32_t>(min(g, p.M - 1));
+    const uint32_t xrows = p.xres ? 4u * p.kw : 4u * S;   // x rows per token in its tile
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    int u = 0;
+    for (int t = 0; t < ntiles; ++t) {
+        const int row0 = r_begin + 16 * t;
         const int ra = min(row0 + g, p.N - 1), rb = min(row0 + g + 8, p.N - 1);
-        const uint32_t offa = static_cast<uint32_t>(((static_cast<int64_t>(ra) * nsb + sb) * BB) & 15);
-        const uint32_t offb = static_cast<uint32_t>(((static_cast<int64_t>(rb) * nsb + sb) * BB) & 15);
-        const uint32_t blk_a = st + g * p.row_pitch + offa;
-        const uint32_t blk_b = st + (g + 8) * p.row_pitch + offb;
-        const uint32_t xb = st + 16 * p.row_pitch + tok * kXTok;
-        if constexpr (TYPE == 12 || TYPE == 13) superblock_kq<TYPE>(blk_a, blk_b, xb, c, acc);
-        else if constexpr (TYPE == 14) superblock_q6(blk_a, blk_b, xb, c, acc);
-        else superblock_iq4(blk_a, blk_b, xb, c, acc);
-        __syncwarp();
-        if (it + D < nmine) {
-            fence_proxy_async_smem();
-            issue(s, sb_begin + it + D);
+        for (int si = 0; si < nst; ++si, ++u) {
+            const int s = u % D;
+            if (ok && !mbar_wait(bar0 + 8 * s, (u / D) & 1)) ok = false;
+            if (ok) {
+                const uint32_t wst = wslot(s);
+                const uint32_t xst = p.xres ? xreg : xslot(s);
+                const int sb0 = kb0 + si * S;
+                const int ns = min(S, kb1 - sb0);
+                const uint32_t xsb0 = p.xres ? static_cast<uint32_t>(si * S) : 0u;   // x superblock index base
+                uint32_t base_a = wst + g * p.row_pitch, base_b = wst + (g + 8) * p.row_pitch;
+                if constexpr (!TMA) {   // block data starts (o & 15) bytes into the row's window
+                    base_a += (static_cast<uint32_t>(ra * p.nsb + sb0) * static_cast<uint32_t>(BB)) & 15u;
+                    base_b += (static_cast<uint32_t>(rb * p.nsb + sb0) * static_cast<uint32_t>(BB)) & 15u;
+                }
+                for (int j = 0; j < ns; ++j) {
+                    const uint32_t blk_a = base_a + j * BB, blk_b = base_b + j * BB;
+                    const uint32_t r0 = tok * xrows + 4u * (xsb0 + j);   // x row of segment 0
+                    if constexpr (TYPE == 12 || TYPE == 13) superblock_kq<TYPE>(blk_a, blk_b, xrow(xst, r0 + c), c, acc);
+                    else if constexpr (TYPE == 14) superblock_q6(blk_a, blk_b, xst, r0, c, acc);
+                    else superblock_iq4(blk_a, blk_b, xrow(xst, r0 + c), c, acc);
+                }
+            }
+            __syncwarp();
+            if (ok && u + D < total) {
+                fence_proxy_async_smem();
+                issue(s, u + D);
+            }
+        }
+        // fixed-order reduction of the warps' 16 x 8 tiles of this row tile
+        float *rt = red + (t & 1) * nwarps * 128;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rt[(warp * 32 + lane) * 4 + i] = acc[i];
+        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+        __syncthreads();
+        for (int q = threadIdx.x; q < 16 * p.M; q += blockDim.x) {
+            const int row = q & 15, tk = q >> 4;
+            const int src_lane = (row & 7) * 4 + (tk >> 1);
+            const int slot = ((row >> 3) << 1) | (tk & 1);
+            float sum = 0.f;
+            for (int w = 0; w < nwarps; ++w) sum += rt[(w * 32 + src_lane) * 4 + slot];
+            if (row0 + row < r_end) p.y[static_cast<int64_t>(tk) * p.N + row0 + row] = sum;
         }
     }
     if (!ok) {
         if (lane == 0) atomicOr(p.status, kStatusTimeout);
         // let copies still in flight land before the shared memory is released
-        for (int j = it + 1; j < nmine && j < it + D; ++j) (void)mbar_wait(bar0 + 8 * (j % D), (j / D) & 1);
-    }
-
-    // fixed-order reduction of the warps' 16 x 8 tiles
-#pragma unroll
-    for (int i = 0; i < 4; ++i) red[(warp * 32 + lane) * 4 + i] = acc[i];
-    __syncthreads();
-    for (int t = threadIdx.x; t < 16 * p.M; t += blockDim.x) {
-        const int row = t & 15, tk = t >> 4;
-        const int src_lane = (row & 7) * 4 + (tk >> 1);
-        const int slot = ((row >> 3) << 1) | (tk & 1);
-        float s = 0.f;
-        for (int w = 0; w < nwarps; ++w) s += red[(w * 32 + src_lane) * 4 + slot];
-        if (row0 + row < p.N) p.y[static_cast<int64_t>(tk) * p.N + row0 + row] = s;
+        for (int j = u; j < total && j < u + D; ++j) (void)mbar_wait(bar0 + 8 * (j % D), (j / D) & 1);
     }
 }
 
 // ---------------------------------------------------------------- host side
 
-namespace {
-template <int TYPE>
-cudaError_t launch_t(const GemvArgs &a, int threads, size_t smem, cudaStream_t stream) {
+struct GemvPlan {
+    GemvArgs a;
+    bool tma;
+    int warps, grid;
+    size_t smem;
+};
+
+GemvPlan make_plan(int type, int64_t N, int64_t K, int M, int num_sms) {
+    GemvPlan pl{};
+    GemvArgs &a = pl.a;
+    const int bb = block_bytes_of(type);
+    const int nsb = static_cast<int>(K / 256);
+    const int64_t row_bytes = static_cast<int64_t>(nsb) * bb;
+    // 2-D tensor copies need 16-byte row strides and box widths; IQ4_XS stages hold an even
+    // number of 136-byte blocks.
+    const int s_mult = (type == 23) ? 2 : 1;
+    pl.tma = (row_bytes % 16 == 0) && type != 14 && (type != 23 || nsb % 2 == 0);
+    const int s_max = pl.tma ? std::max(s_mult, (2048 / bb) / s_mult * s_mult) : 8;   // <= 2 KB per row
+    auto pitch_of = [&](int S) {
+        if (pl.tma) return static_cast<uint32_t>(S * bb);   // dense rows as the tensor copy lands them
+        uint32_t pitch = static_cast<uint32_t>((S * bb + 30) & ~15);   // window incl. misalignment
+        if ((pitch / 16) % 2 == 0) pitch += 16;                         // odd multiple of 16
+        return pitch;
+    };
+    // K slice per warp: up to 16 warps, slices a multiple of s_mult superblocks
+    int w = std::max(1, std::min(16, nsb / s_mult));
+    int kw = (nsb + w - 1) / w;
+    kw = (kw + s_mult - 1) / s_mult * s_mult;
+    w = (nsb + kw - 1) / kw;
+    const size_t limit = 227 * 1024;
+    auto layout = [&](bool xres, int S, int D, GemvArgs &o) {
+        o.S = S;
+        o.stages = D;
+        o.row_pitch = pitch_of(S);
+        o.w_bytes = 16 * o.row_pitch;
+        o.x_tx = static_cast<uint32_t>(M * (xres ? kw : S) * 512);
+        o.x_bytes = xres ? 0u : o.x_tx;
+        o.x_warp_bytes = xres ? ((o.x_tx + 1023u) & ~1023u) : 0u;
+        o.slot_bytes = (o.x_bytes + o.w_bytes + 1023u) & ~1023u;
+        o.xres = xres ? 1 : 0;
+        const uint32_t bars = static_cast<uint32_t>((w * (D + 1) * 8 + 1023) & ~1023);
+        o.red_offset = bars;
+        o.x_offset = (bars + static_cast<uint32_t>(2 * w * 128 * sizeof(float)) + 1023u) & ~1023u;
+        o.ring_offset = o.x_offset + w * o.x_warp_bytes;
+        return static_cast<size_t>(1024) + o.ring_offset + static_cast<size_t>(w) * D * o.slot_bytes;
+    };
+    size_t smem = 0;
+    bool found = false;
+    for (int xres = 1; xres >= 0 && !found; --xres) {
+        for (int S = std::min(kw, s_max); S >= s_mult && !found; S -= s_mult) {
+            const int nst = (kw + S - 1) / S;
+            for (int D = std::min(4, std::max(2, 2 * nst)); D >= 2 && !found; --D) {
+                smem = layout(xres == 1, S, D, a);
+                found = smem <= limit;
+            }
+        }
+    }
+    if (!found) {
+        pl.smem = SIZE_MAX;
+        return pl;
+    }
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.M = M;
+    a.nsb = nsb;
+    a.kw = kw;
+    a.total_bytes = static_cast<int64_t>(N) * row_bytes;
+    pl.warps = w;
+    pl.grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(num_sms, (N + 15) / 16)));
+    pl.smem = smem;
+    return pl;
+}
+
+template <int TYPE, bool TMA>
+cudaError_t launch_t(const CUtensorMap &wm, const CUtensorMap &xm, const GemvArgs &a, int grid, int threads,
+                     size_t smem, cudaStream_t st) {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_kernel<TYPE>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        cudaError_t e = cudaFuncSetAttribute(gemv_kernel<TYPE, TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             227 * 1024);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    const int grid = (a.N + 15) / 16;
-    gemv_kernel<TYPE><<<grid, threads, smem, stream>>>(a);
+    gemv_kernel<TYPE, TMA><<<grid, threads, smem, st>>>(wm, xm, a);
     return cudaGetLastError();
 }
+
+template <int TYPE>
+cudaError_t launch_type(bool tma, const CUtensorMap &wm, const CUtensorMap &xm, const GemvArgs &a, int grid,
+                        int threads, size_t smem, cudaStream_t st) {
+    return tma ? launch_t<TYPE, true>(wm, xm, a, grid, threads, smem, st)
+               : launch_t<TYPE, false>(wm, xm, a, grid, threads, smem, st);
+}
+
 }  // namespace
-
-int gemv_block_bytes(int type) {
-    switch (type) {
-    case 12: return 144;
-    case 13: return 176;
-    case 14: return 210;
-    case 23: return 136;
-    default: return -1;
-    }
-}
-
-// Choose warps per CTA and pipeline depth: enough warps GPU-wide to cover HBM latency
-// (about 16 per SM), no more warps than superblocks, and shared memory within budget.
-GemvPlan gemv_plan(int type, int64_t N, int64_t K, int M, int num_sms) {
-    GemvPlan pl{};
-    const int bb = gemv_block_bytes(type);
-    const int nsb = static_cast<int>(K / 256);
-    const int tiles = static_cast<int>((N + 15) / 16);
-    const uint32_t pitch_raw = static_cast<uint32_t>((bb + 15 + 15) & ~15);   // window incl. misalignment
-    // odd multiple of 16 bytes -> row groups g, g+1 start on different bank quarters
-    pl.row_pitch = ((pitch_raw / 16) % 2 == 1) ? pitch_raw : pitch_raw + 16;
-    if (type == 12 || type == 13) pl.row_pitch = ((static_cast<uint32_t>(bb) / 16) % 2 == 1) ? bb : bb + 16;
-    pl.stage_bytes = 16 * pl.row_pitch + M * kXTok;
-    const int want_warps = 16 * num_sms;
-    int w = 1;
-    while (w < 16 && w * tiles < want_warps) w *= 2;
-    while (w > 1 && w > nsb) w /= 2;
-    int D = 4;
-    auto smem_of = [&](int ww, int dd) {
-        const size_t bars = ((static_cast<size_t>(ww) * dd * 8) + 127) & ~size_t(127);
-        const size_t red = static_cast<size_t>(ww) * 32 * 4 * sizeof(float);
-        return bars + red + static_cast<size_t>(ww) * dd * pl.stage_bytes;
-    };
-    const size_t budget = 200 * 1024;
-    while (smem_of(w, D) > budget && D > 2) --D;
-    while (smem_of(w, D) > budget && w > 1) w /= 2;
-    pl.warps = w;
-    pl.stages = D;
-    pl.sb_per_warp = (nsb + w - 1) / w;
-    pl.red_offset = static_cast<uint32_t>(((static_cast<size_t>(w) * D * 8) + 127) & ~size_t(127));
-    pl.region_offset = pl.red_offset + static_cast<uint32_t>(w * 32 * 4 * sizeof(float));
-    pl.warp_bytes = D * pl.stage_bytes;
-    pl.smem = smem_of(w, D);
-    pl.grid = tiles;
-    return pl;
-}
 
 cudaError_t gemv_launch(int type, const uint8_t *W, const __half *x, float *y, int64_t N, int64_t K, int M,
                         unsigned *status, int num_sms, cudaStream_t stream) {
-    const GemvPlan pl = gemv_plan(type, N, K, M, num_sms);
-    GemvArgs a{};
-    a.W = W;
-    a.x = x;
-    a.y = y;
-    a.status = status;
-    a.N = static_cast<int>(N);
-    a.K = static_cast<int>(K);
-    a.M = M;
-    a.nsb = static_cast<int>(K / 256);
-    a.sb_per_warp = pl.sb_per_warp;
-    a.stages = pl.stages;
-    a.row_pitch = pl.row_pitch;
-    a.stage_bytes = pl.stage_bytes;
-    a.warp_bytes = pl.warp_bytes;
-    a.red_offset = pl.red_offset;
-    a.region_offset = pl.region_offset;
-    a.total_bytes = N * (K / 256) * gemv_block_bytes(type);
+    const int bb = block_bytes_of(type);
+    if (bb < 0 || M < 1 || M > kGemvMaxM) return cudaErrorInvalidValue;
+    GemvPlan pl = make_plan(type, N, K, M, num_sms);
+    if (pl.smem > 227 * 1024) return cudaErrorNotSupported;
+    pl.a.W = W;
+    pl.a.x = x;
+    pl.a.y = y;
+    pl.a.status = status;
+    CUtensorMap wm{}, xm{};
+    // x viewed as [M tokens][K/64 rows][64 halves]; one box = all tokens x (4 rows per
+    // superblock of a warp slice or of a stage), 128-byte swizzled
+    const uint32_t xbox_rows = static_cast<uint32_t>(4 * (pl.a.xres ? pl.a.kw : pl.a.S));
+    if (!encode_tmap_3d(&xm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, 64, static_cast<uint64_t>(K / 64),
+                        static_cast<uint64_t>(M), 128, static_cast<uint64_t>(K) * 2, 64, xbox_rows,
+                        static_cast<uint32_t>(M), true))
+        return cudaErrorInvalidValue;
+    if (pl.tma) {   // W viewed as [N rows][row bytes / 8] of 8-byte elements
+        const uint64_t row_elems = static_cast<uint64_t>(K / 256) * bb / 8;
+        if (!encode_tmap_2d(&wm, CU_TENSOR_MAP_DATA_TYPE_UINT64, W, row_elems, static_cast<uint64_t>(N), row_elems * 8,
+                            static_cast<uint32_t>(pl.a.S * bb / 8), 16, false))
+            return cudaErrorInvalidValue;
+    }
     const int threads = 32 * pl.warps;
     switch (type) {
-    case 12: return launch_t<12>(a, threads, pl.smem, stream);
-    case 13: return launch_t<13>(a, threads, pl.smem, stream);
-    case 14: return launch_t<14>(a, threads, pl.smem, stream);
-    case 23: return launch_t<23>(a, threads, pl.smem, stream);
+    case 12: return launch_type<12>(pl.tma, wm, xm, pl.a, pl.grid, threads, pl.smem, stream);
+    case 13: return launch_type<13>(pl.tma, wm, xm, pl.a, pl.grid, threads, pl.smem, stream);
+    case 14: return launch_type<14>(pl.tma, wm, xm, pl.a, pl.grid, threads, pl.smem, stream);
+    case 23: return launch_type<23>(pl.tma, wm, xm, pl.a, pl.grid, threads, pl.smem, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -8,35 +8,15 @@
 
 namespace ql {
 
+// Bytes per 256-weight superblock of a ggml type id (Q4_K 144, Q5_K 176, Q6_K 210,
+// IQ4_XS 136), or -1.
+int block_bytes_of(int type);
+
 // ---------------------------------------------------------------- decode GEMV (gemv.cu)
-
-struct GemvArgs {
-    const uint8_t *W;
-    const __half *x;
-    float *y;
-    unsigned *status;
-    int N, K, M;          // M <= 8
-    int nsb;              // K / 256
-    int sb_per_warp;      // contiguous superblocks per warp
-    int stages;           // ring depth per warp
-    uint32_t row_pitch;   // bytes per weight row in a stage (multiple of 16)
-    uint32_t stage_bytes; // 16 * row_pitch + M * 576
-    uint32_t warp_bytes;  // stages * stage_bytes
-    uint32_t red_offset;  // byte offset of the reduction area in dynamic shared memory
-    uint32_t region_offset;
-    int64_t total_bytes;  // size of W in bytes
-};
-
-struct GemvPlan {
-    int warps, stages, sb_per_warp, grid;
-    uint32_t row_pitch, stage_bytes, warp_bytes, red_offset, region_offset;
-    size_t smem;
-};
 
 constexpr int kGemvMaxM = 8;
 
-int gemv_block_bytes(int type);
-GemvPlan gemv_plan(int type, int64_t N, int64_t K, int M, int num_sms);
+// y[M <= 8, N] = x . dequant(W)^T, one launch.
 cudaError_t gemv_launch(int type, const uint8_t *W, const __half *x, float *y, int64_t N, int64_t K, int M,
                         unsigned *status, int num_sms, cudaStream_t stream);
 
@@ -47,5 +27,15 @@ cudaError_t gemv_launch(int type, const uint8_t *W, const __half *x, float *y, i
 cudaError_t gemm_launch(int type, const uint8_t *W, const __half *x, float *y, int64_t N, int64_t K, int64_t M,
                         unsigned *status, int num_sms, cudaStream_t stream);
 int gemm_launch_count(int type, int64_t N, int64_t K, int64_t M);
+
+// ---------------------------------------------------------------- tensor maps (tmap.cu)
+
+// Encode a 2-D tiled tensor map (no swizzle unless `swizzle128`); false if the driver
+// entry point is unavailable or the encoding is rejected.
+bool encode_tmap_2d(void *tmap_out, int dtype /* CUtensorMapDataType */, const void *base, uint64_t dim0,
+                    uint64_t dim1, uint64_t stride1_bytes, uint32_t box0, uint32_t box1, bool swizzle128);
+bool encode_tmap_3d(void *tmap_out, int dtype, const void *base, uint64_t dim0, uint64_t dim1, uint64_t dim2,
+                    uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1, uint32_t box2,
+                    bool swizzle128);
 
 }  // namespace ql

@@ -59,7 +59,7 @@ int device_state(DeviceState **out) {
 }
 
 int validate(int type, const void *W, int64_t N, int64_t K, const void *x, int64_t M, const float *y) {
-    if (ql::gemv_block_bytes(type) < 0) return QL_ERR_TYPE;
+    if (ql::block_bytes_of(type) < 0) return QL_ERR_TYPE;
     if (N < 1 || M < 1 || K < 256 || K % 256 != 0) return QL_ERR_SHAPE;
     // 32-bit indexing limits inside the kernels
     if (N > (int64_t(1) << 30) || K > (int64_t(1) << 24) || M > (int64_t(1) << 24)) return QL_ERR_SHAPE;
@@ -120,7 +120,7 @@ int qlinear_gemm(int type, const void *W_blocks, int64_t N, int64_t K, const voi
 }
 
 int qlinear_block_bytes(int type) {
-    const int b = ql::gemv_block_bytes(type);
+    const int b = ql::block_bytes_of(type);
     return b < 0 ? QL_ERR_TYPE : b;
 }
 
@@ -156,7 +156,7 @@ int qlinear_device_status(void *stream) {
 }
 
 int qlinear_launch_count(int type, int64_t N, int64_t K, int64_t M) {
-    if (ql::gemv_block_bytes(type) < 0) return QL_ERR_TYPE;
+    if (ql::block_bytes_of(type) < 0) return QL_ERR_TYPE;
     if (N < 1 || M < 1 || K < 256 || K % 256 != 0) return QL_ERR_SHAPE;
     if (M <= ql::kGemvMaxM) return 1;
     return ql::gemm_launch_count(type, N, K, M);

@@ -107,8 +107,9 @@ def test_zero_weights_and_zero_activations(ql, path, t):
 
 @pytest.mark.parametrize("t", TYPES)
 def test_unit_activation_picks_a_column(ql, t):
-    """x = e_k: the decode kernel returns column k of dequant(W). It multiplies exact
-    integer-valued fp16 operands and scales in fp32, so the only error is fp32 rounding."""
+    """x = e_k: the decode kernel returns column k of dequant(W). Its fp16 MMA operand is the
+    integer sc*q (K-quants, |.| <= 1953: exact), sc*(q-32) (Q6_K) or (ls-32)*codebook[q]
+    (IQ4_XS, |.| <= 4064: rounded to 11 significant bits when above 2048), scaled in fp32."""
     N, K = 70, 768
     W = synth.weights(t, N, K, [410, t])
     w = oracle.dequant(t, W, N, K)
@@ -118,7 +119,8 @@ def test_unit_activation_picks_a_column(ql, t):
         x[i, k] = 1.0
     y = run(ql, "gemv", t, W, N, K, x)
     ref = w[:, ks].T
-    np.testing.assert_allclose(y, ref, rtol=2 ** -20, atol=2 ** -40)
+    rtol = 2 ** -11 if t in (14, 23) else 2 ** -20   # one fp16 rounding of the integer operand
+    np.testing.assert_allclose(y, ref, rtol=rtol, atol=2 ** -40)
 
 
 @pytest.mark.parametrize("path", ["gemv", "gemm"])

@@ -88,7 +88,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -164,11 +164,13 @@ def run_ours(args, rank, world, local_rank):
             step(i)
     torch.cuda.synchronize(dev)
 
-    # Capture the K timed steps as one CUDA graph (launch-bound otherwise: a decode GEMV
-    # is a few microseconds); replay it once untimed, then time one replay.
+    # The timed steps run as replays of one CUDA graph holding `chunk` steps (a decode GEMV
+    # is a few microseconds: launched one by one from Python the GPU would idle), chunk
+    # dividing K so that exactly K steps are timed; one untimed replay first.
+    chunk = next(d for d in range(min(args.steps, 200), 0, -1) if args.steps % d == 0)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
-        for i in range(args.steps):
+        for i in range(chunk):
             step(i)
     with torch.cuda.stream(stream):
         g.replay()
@@ -181,7 +183,8 @@ def run_ours(args, rank, world, local_rank):
         time.sleep(0.05)
         with torch.cuda.stream(stream):
             e0.record(stream)
-            g.replay()
+            for _ in range(args.steps // chunk):
+                g.replay()
             e1.record(stream)
         torch.cuda.synchronize(dev)
     if world > 1:
@@ -323,32 +326,49 @@ def cpu_baseline(budget_s=12.0):
 
 
 def run_reference(args):
-    """--impl reference: the oracle on the host cores, same metric and workload."""
-    cores = len(os.sched_getaffinity(0))
+    """--impl reference: the oracle on the host cores, same metric and workload. Each step
+    runs the oracle over the first R rows of every layer shape (R calibrated once so that the
+    whole run stays within a few minutes) and the value is that sample's GB/s."""
     import oracle
     oracle.build()
-    per_step = []
+    cores = len(os.sched_getaffinity(0))
+    per_step_s = max(0.05, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
+    samples = []
+    for i, (K, N) in enumerate(DECODE_SHAPES):
+        x = synth.activations(DECODE_M, K, [12, i])
+        rows = max(cores, 32)
+        W = synth.weights(DECODE_TYPE, rows, K, [11, i])
+        t0 = time.perf_counter()
+        oracle.qlinear(DECODE_TYPE, W, rows, K, x, n_threads=cores)
+        dt = max(time.perf_counter() - t0, 1e-6)
+        rows = int(max(cores, min(N, rows * (per_step_s / 4) / dt)))
+        samples.append((K, rows, synth.weights(DECODE_TYPE, rows, K, [11, i]), x))
+    vals = []
     for s in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        cb = cpu_baseline(budget_s=args.cpu_budget / max(1, args.steps))
+        nbytes = 0
+        for K, rows, W, x in samples:
+            oracle.qlinear(DECODE_TYPE, W, rows, K, x, n_threads=cores)
+            nbytes += alg_bytes(DECODE_TYPE, K, rows, DECODE_M)
+        dt = time.perf_counter() - t0
         if s >= args.warmup:
-            per_step.append(cb["value"])
-    v = float(np.median(per_step))
+            vals.append(nbytes / dt / 1e9)
+    v = float(np.median(vals))
+    sample = f"first {[r for _, r, _, _ in samples]} rows of the four (K,N) decode shapes per step, M=1, fp64"
     return {"metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": {"workload": "Q4_K decode, 8B-class layer: M=1, (K,N) in (4096,4096),(4096,1024),(4096,12288),(12288,4096)",
                        "parallelism": "host cores"},
-            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                             "sample": cb["sample"]},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args()

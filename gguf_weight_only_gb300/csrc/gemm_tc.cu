@@ -47,7 +47,8 @@ struct GemmArgs {
     int S;                     // superblocks per weight stage
     uint32_t row_pitch;        // bytes per weight row in a weight stage
     int qstages, bstages;
-    uint32_t q_stage_bytes, b_stage_bytes;
+    int xk;                    // 64-wide chunks per activation stage (1, 2 or 4)
+    uint32_t q_stage_bytes, b_stage_bytes;   // b stage = xk boxes of n_tile x 128 bytes
     uint32_t q_off, bar_off;   // offsets from the 1024-aligned shared base
     int64_t total_bytes;
     int bb;                    // bytes per superblock
@@ -203,17 +204,16 @@ __device__ __forceinline__ void iq4_chunk(uint32_t blk, int gg, int h, uint32_t 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
                                               unsigned *status) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait_for(bar, parity, 100000u)) {
         if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (clock64() - t0 > kWaitLimitCycles) {
             *abort_flag = 1u;
             atomicOr(status, kStatusTimeout);
             return false;
         }
     }
+    return true;
 }
 
 }  // namespace
@@ -273,6 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // The weights stream while the preceding kernel in the stream finishes; x is loaded (and
+    // y written, downstream of x) only after it has completed.
+    pdl_launch_dependents();
 
     if (warp < kDequantWarps) {
         // ---------------------------------------------------- dequantisers
@@ -401,13 +404,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 9) {
         // ---------------------------------------------------- activation producer
         if (lane == 0) {
+            pdl_wait();
             int issued = 0;
-            for (int chunk = 0; chunk < nchunks; ++chunk) {
-                const int s = chunk % BS;
-                if (!wait_or_abort(bempty(s), ((chunk / BS) & 1) ^ 1, abort_flag, p.status)) break;
-                mbar_arrive_expect_tx(bfull(s), p.b_stage_bytes);
-                tma_load_2d(b_ring + s * p.b_stage_bytes, &xmap, chunk * kChunkK, t0, bfull(s));
-                issued = chunk + 1;
+            const int nx = (nchunks + p.xk - 1) / p.xk;
+            const uint32_t box_bytes = static_cast<uint32_t>(p.n_tile) * 128u;
+            for (int xs = 0; xs < nx; ++xs) {
+                const int s = xs % BS;
+                if (!wait_or_abort(bempty(s), ((xs / BS) & 1) ^ 1, abort_flag, p.status)) break;
+                const int nb = min(p.xk, nchunks - xs * p.xk);
+                mbar_arrive_expect_tx(bfull(s), nb * box_bytes);
+                for (int i = 0; i < nb; ++i)
+                    tma_load_2d(b_ring + s * p.b_stage_bytes + i * box_bytes, &xmap, (xs * p.xk + i) * kChunkK, t0,
+                                bfull(s));
+                issued = xs + 1;
             }
             if (*abort_flag) {
                 for (int c = max(0, issued - BS); c < issued; ++c) (void)mbar_wait(bfull(c % BS), (c / BS) & 1);
@@ -418,21 +427,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint32_t idesc = idesc_f16_f32(kRows, p.n_tile);
             bool ok = true;
+            const uint32_t box_bytes = static_cast<uint32_t>(p.n_tile) * 128u;
             for (int chunk = 0; chunk < nchunks; ++chunk) {
-                const int sa = chunk % kAStages, sbb = chunk % BS;
+                const int sa = chunk % kAStages;
+                const int xs = chunk / p.xk, xi = chunk - xs * p.xk, sbb = xs % BS;
                 if (!wait_or_abort(afull(sa), (chunk / kAStages) & 1, abort_flag, p.status) ||
-                    !wait_or_abort(bfull(sbb), (chunk / BS) & 1, abort_flag, p.status)) {
+                    (xi == 0 && !wait_or_abort(bfull(sbb), (xs / BS) & 1, abort_flag, p.status))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t bst = b_ring + sbb * p.b_stage_bytes;
+                const uint32_t bst = b_ring + sbb * p.b_stage_bytes + xi * box_bytes;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     tc_mma_ts(tmem, tmem + kACol + sa * 32 + kk * 8, smem_desc_sw128(bst + 32 * kk), idesc,
                               (chunk | kk) != 0);
                 tc_commit(aempty(sa));
-                tc_commit(bempty(sbb));
+                if (xi == p.xk - 1 || chunk == nchunks - 1) tc_commit(bempty(sbb));
             }
             tc_commit(accfull);   // also drains in-flight MMAs on the abort path
             if (!ok) (void)mbar_wait(accfull, 0);
@@ -458,7 +469,7 @@ int pick_n_tile(int64_t M) {
 }
 
 struct GemmPlan {
-    int n_tile, qstages, bstages, S;
+    int n_tile, qstages, bstages, S, xk;
     bool tma;
     uint32_t row_pitch, q_stage_bytes, b_stage_bytes, q_off, bar_off;
     size_t smem;
@@ -479,10 +490,12 @@ GemmPlan gemm_plan(int type, int bb, int64_t K, int64_t M) {
     }
     pl.row_pitch = pitch;
     pl.q_stage_bytes = kRows * pitch;
-    pl.b_stage_bytes = static_cast<uint32_t>(pl.n_tile) * 128u;
+    // activation stages of about 32 KB: 1, 2 or 4 chunks of 64 columns
+    pl.xk = pl.n_tile >= 256 ? 1 : pl.n_tile >= 128 ? 2 : 4;
+    pl.b_stage_bytes = static_cast<uint32_t>(pl.n_tile) * 128u * pl.xk;
     const size_t limit = 227 * 1024 - 1024;
     for (int bs = 4; bs >= 2; --bs) {
-        for (int qs = 3; qs >= 2; --qs) {
+        for (int qs = 8; qs >= 2; --qs) {
             const size_t q_off = static_cast<size_t>(bs) * pl.b_stage_bytes;
             const size_t bar_off = (q_off + static_cast<size_t>(qs) * pl.q_stage_bytes + 15) & ~size_t(15);
             const size_t total = bar_off + 8 * (2 * qs + 2 * bs + 2 * kAStages + 1) + 16;
@@ -502,25 +515,25 @@ GemmPlan gemm_plan(int type, int bb, int64_t K, int64_t M) {
 
 template <int TYPE, bool TMA>
 cudaError_t launch_t(const CUtensorMap &xmap, const CUtensorMap &wmap, const GemmArgs &a, dim3 grid, size_t smem,
-                     cudaStream_t st) {
+                     bool pdl, cudaStream_t st) {
+    auto kern = gemm_kernel<TYPE, TMA>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e =
-            cudaFuncSetAttribute(gemm_kernel<TYPE, TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    gemm_kernel<TYPE, TMA><<<grid, kThreads, smem, st>>>(xmap, wmap, a);
-    return cudaGetLastError();
+    void *args[] = {const_cast<CUtensorMap *>(&xmap), const_cast<CUtensorMap *>(&wmap), const_cast<GemmArgs *>(&a)};
+    return launch_pdl(reinterpret_cast<const void *>(kern), grid, dim3(kThreads), smem, st, pdl, args);
 }
 
 template <int TYPE>
 cudaError_t launch_type(bool tma, const CUtensorMap &xmap, const CUtensorMap &wmap, const GemmArgs &a, dim3 grid,
-                        size_t smem, cudaStream_t st) {
-    return tma ? launch_t<TYPE, true>(xmap, wmap, a, grid, smem, st)
-               : launch_t<TYPE, false>(xmap, wmap, a, grid, smem, st);
+                        size_t smem, bool pdl, cudaStream_t st) {
+    return tma ? launch_t<TYPE, true>(xmap, wmap, a, grid, smem, pdl, st)
+               : launch_t<TYPE, false>(xmap, wmap, a, grid, smem, pdl, st);
 }
 
 }  // namespace
@@ -528,7 +541,7 @@ cudaError_t launch_type(bool tma, const CUtensorMap &xmap, const CUtensorMap &wm
 int gemm_launch_count(int, int64_t, int64_t, int64_t) { return 1; }
 
 cudaError_t gemm_launch(int type, const uint8_t *W, const __half *x, float *y, int64_t N, int64_t K, int64_t M,
-                        unsigned *status, int, cudaStream_t stream) {
+                        unsigned *status, int, bool pdl, cudaStream_t stream) {
     const int bb = block_bytes_of(type);
     if (bb < 0) return cudaErrorInvalidValue;
     const GemmPlan pl = gemm_plan(type, bb, K, M);
@@ -557,6 +570,7 @@ cudaError_t gemm_launch(int type, const uint8_t *W, const __half *x, float *y, i
     a.row_pitch = pl.row_pitch;
     a.qstages = pl.qstages;
     a.bstages = pl.bstages;
+    a.xk = pl.xk;
     a.q_stage_bytes = pl.q_stage_bytes;
     a.b_stage_bytes = pl.b_stage_bytes;
     a.q_off = pl.q_off;
@@ -566,10 +580,10 @@ cudaError_t gemm_launch(int type, const uint8_t *W, const __half *x, float *y, i
     a.type = type;
     const dim3 grid(static_cast<unsigned>((N + kRows - 1) / kRows), static_cast<unsigned>((M + pl.n_tile - 1) / pl.n_tile));
     switch (type) {
-    case 12: return launch_type<12>(pl.tma, xmap, wmap, a, grid, pl.smem, stream);
-    case 13: return launch_type<13>(pl.tma, xmap, wmap, a, grid, pl.smem, stream);
-    case 14: return launch_type<14>(pl.tma, xmap, wmap, a, grid, pl.smem, stream);
-    case 23: return launch_type<23>(pl.tma, xmap, wmap, a, grid, pl.smem, stream);
+    case 12: return launch_type<12>(pl.tma, xmap, wmap, a, grid, pl.smem, pdl, stream);
+    case 13: return launch_type<13>(pl.tma, xmap, wmap, a, grid, pl.smem, pdl, stream);
+    case 14: return launch_type<14>(pl.tma, xmap, wmap, a, grid, pl.smem, pdl, stream);
+    case 23: return launch_type<23>(pl.tma, xmap, wmap, a, grid, pl.smem, pdl, stream);
     default: return cudaErrorInvalidValue;
     }
 }

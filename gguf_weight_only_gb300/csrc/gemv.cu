@@ -106,19 +106,20 @@ __device__ __forceinline__ KqConsts kq_consts(uint4 h, int c) {
 
 // One qs word of a K-quant row -> the four A pairs (exact sc*q in fp16).
 // w = qs bytes [b0 b1 b2 b3] at positions l..l+3 of 32-byte group c: low nibbles are weights
-// of sub-block 2c, high nibbles of sub-block 2c+1. Reordered to [b0 b2 b1 b3] so that each
-// half lane holds neighbouring positions: pairs (b0, b1) and (b2, b3), i.e. columns (k, k+1).
+// of sub-block 2c, high nibbles of sub-block 2c+1. Masking w pairs the half lanes (b0, b2)
+// and (b1, b3): with x stored permuted ([x0 x2 x1 x3] per group of four, PERM) that is used
+// directly; otherwise w is first reordered to [b0 b2 b1 b3], giving (b0, b1) and (b2, b3).
 // qh (Q5_K only) = qh[l..l+3]; bit 2c / 2c+1 of each byte is the fifth bit.
-template <bool Q5>
+template <bool Q5, bool PERM>
 __device__ __forceinline__ void kq_word(uint32_t w, uint32_t qh, int c, const KqConsts &k, uint32_t &lo01,
                                         uint32_t &lo23, uint32_t &hi01, uint32_t &hi23) {
-    const uint32_t w2 = prmt(w, 0u, 0x3120u), w3 = w2 >> 8;
+    const uint32_t w2 = PERM ? w : prmt(w, 0u, 0x3120u), w3 = w2 >> 8;
     uint32_t l01 = and_or(w2, 0x000F000Fu, kH2_1024);   // (1024 + q)
     uint32_t l23 = and_or(w3, 0x000F000Fu, kH2_1024);
     uint32_t h01 = and_or(w2, 0x00F000F0u, kH2_1024);   // (1024 + 16 q)
     uint32_t h23 = and_or(w3, 0x00F000F0u, kH2_1024);
     if constexpr (Q5) {
-        const uint32_t q2 = prmt(qh, 0u, 0x3120u), q3 = q2 >> 8;
+        const uint32_t q2 = PERM ? qh : prmt(qh, 0u, 0x3120u), q3 = q2 >> 8;
         const uint32_t rl = (4u - 2u * c) & 31u, rh = (7u - 2u * c) & 31u;
         l01 = or_and(l01, rotl(q2, rl), 0x00100010u);   // bit 2c   -> bit 4 (+16)
         l23 = or_and(l23, rotl(q3, rl), 0x00100010u);
@@ -160,7 +161,7 @@ __device__ __forceinline__ uint4 ldx(const XRow &x, uint32_t p) { return lds128(
 
 // Q4_K / Q5_K: lane (g, c) decodes 32-byte qs group c (sub-blocks 2c, 2c+1) of rows g, g+8.
 // xr = row of columns 64c .. 64c+63 of this superblock.
-template <int TYPE>
+template <int TYPE, bool PERM>
 __device__ __forceinline__ void superblock_kq(uint32_t blk_a, uint32_t blk_b, const XRow &xr, int c, float (&acc)[4]) {
     constexpr bool Q5 = (TYPE == 13);
     constexpr uint32_t QS = Q5 ? 48 : 16;
@@ -184,8 +185,8 @@ __device__ __forceinline__ void superblock_kq(uint32_t blk_a, uint32_t blk_b, co
         for (int v = 0; v < 2; ++v) {
             const int uu = u + v;
             uint32_t la01, la23, ha01, ha23, lb01, lb23, hb01, hb23;
-            kq_word<Q5>(word_of(qa0, qa1, uu), word_of(ha0, ha1, uu), c, ka, la01, la23, ha01, ha23);
-            kq_word<Q5>(word_of(qb0, qb1, uu), word_of(hb0, hb1, uu), c, kb, lb01, lb23, hb01, hb23);
+            kq_word<Q5, PERM>(word_of(qa0, qa1, uu), word_of(ha0, ha1, uu), c, ka, la01, la23, ha01, ha23);
+            kq_word<Q5, PERM>(word_of(qb0, qb1, uu), word_of(hb0, hb1, uu), c, kb, lb01, lb23, hb01, hb23);
             const uint32_t x0 = v ? xl.z : xl.x, x1 = v ? xl.w : xl.y;
             const uint32_t y0 = v ? xh.z : xh.x, y1 = v ? xh.w : xh.y;
             mma16816(d1, la01, lb01, la23, lb23, x0, x1);
@@ -231,11 +232,13 @@ __device__ __forceinline__ void q6_row_consts(uint32_t blk, int h, int e, uint32
     d = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(blk + 208))));
 }
 
-// A pairs of quarter t for one (ql word, qh word): columns (k0, k0+1), (k0+2, k0+3) as sc*(q-32).
+// A pairs of quarter t for one (ql word, qh word) as sc*(q-32): columns (k0, k0+2) and
+// (k0+1, k0+3) with permuted x (PERM), else (k0, k0+1) and (k0+2, k0+3).
+template <bool PERM>
 __device__ __forceinline__ void q6_pairs(uint32_t qlw, uint32_t qhw, int t, uint32_t sc, uint32_t &p01, uint32_t &p23) {
-    uint32_t l2 = prmt(qlw, 0u, 0x3120u);
+    uint32_t l2 = PERM ? qlw : prmt(qlw, 0u, 0x3120u);
     if (t >= 2) l2 >>= 4;
-    const uint32_t h2 = prmt(qhw, 0u, 0x3120u);
+    const uint32_t h2 = PERM ? qhw : prmt(qhw, 0u, 0x3120u);
     uint32_t v01 = and_or(l2, 0x000F000Fu, kH2_1024);
     uint32_t v23 = and_or(l2 >> 8, 0x000F000Fu, kH2_1024);
     // bits 2t, 2t+1 of each qh byte -> bits 4, 5 of the half
@@ -248,6 +251,7 @@ __device__ __forceinline__ void q6_pairs(uint32_t qlw, uint32_t qhw, int t, uint
 }
 
 // xs = x tile of this stage, r0 = token row base (tok * 4S + 4j).
+template <bool PERM>
 __device__ __forceinline__ void superblock_q6(uint32_t blk_a, uint32_t blk_b, uint32_t xs, uint32_t r0, int c,
                                               float (&acc)[4]) {
     const int h = c >> 1, e = c & 1;
@@ -270,8 +274,8 @@ __device__ __forceinline__ void superblock_q6(uint32_t blk_a, uint32_t blk_b, ui
             for (int v = 0; v < 2; ++v) {
                 const int uu = u + v;
                 uint32_t a01, a23, b01, b23;
-                q6_pairs(word4((t & 1) ? qaB : qaA, uu), word4(qaH, uu), t, sca[t], a01, a23);
-                q6_pairs(word4((t & 1) ? qbB : qbA, uu), word4(qbH, uu), t, scb[t], b01, b23);
+                q6_pairs<PERM>(word4((t & 1) ? qaB : qaA, uu), word4(qaH, uu), t, sca[t], a01, a23);
+                q6_pairs<PERM>(word4((t & 1) ? qbB : qbA, uu), word4(qbH, uu), t, scb[t], b01, b23);
                 mma16816(d1, a01, b01, a23, b23, v ? xv.z : xv.x, v ? xv.w : xv.y);
             }
         }
@@ -369,10 +373,11 @@ __device__ __forceinline__ void superblock_iq4(uint32_t blk_a, uint32_t blk_b, c
 // unit as soon as it has consumed it, across tile boundaries. After each tile the warps'
 // 16 x 8 partial tiles are summed in fixed order through shared memory.
 
-template <int TYPE, bool TMA>
+template <int TYPE, bool TMA, bool XRES>
 __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ CUtensorMap wmap,
                                                       const __grid_constant__ CUtensorMap xmap, const GemvArgs p) {
     constexpr int BB = GemvFmt<TYPE>::BB;
+    constexpr bool PERM = XRES && TYPE != 23;   // resident x is permuted once for the K-quant/Q6_K pairing
     extern __shared__ __align__(1024) uint8_t smem[];
     const int nwarps = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -409,7 +414,7 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ CU
     __syncwarp();
 
     // x slot of a ring slot (per-stage x) sits in front of its weights
-    auto wslot = [&](int s) { return ring + s * p.slot_bytes + (p.xres ? 0u : p.x_bytes); };
+    auto wslot = [&](int s) { return ring + s * p.slot_bytes + (XRES ? 0u : p.x_bytes); };
     auto xslot = [&](int s) { return ring + s * p.slot_bytes; };
 
     auto issue = [&](int s, int u) {
@@ -417,12 +422,12 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ CU
         const int sb = kb0 + si * S;
         const int row0 = r_begin + 16 * t;
         const uint32_t bar = bar0 + 8 * s;
-        const uint32_t xtx = p.xres ? 0u : p.x_tx;
+        const uint32_t xtx = XRES ? 0u : p.x_tx;
         if constexpr (TMA) {
             if (lane == 0) {
                 mbar_arrive_expect_tx(bar, p.w_bytes + xtx);
                 tma_load_2d(wslot(s), &wmap, sb * (BB / 8), row0, bar);
-                if (!p.xres) tma_load_3d(xslot(s), &xmap, 0, sb * 4, 0, bar);
+                if (!XRES) tma_load_3d(xslot(s), &xmap, 0, sb * 4, 0, bar);
             }
         } else {
             const int ns = min(S, kb1 - sb);
@@ -453,23 +458,41 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ CU
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive_expect_tx(bar, sum + xtx);
-                if (!p.xres) tma_load_3d(xslot(s), &xmap, 0, sb * 4, 0, bar);
+                if (!XRES) tma_load_3d(xslot(s), &xmap, 0, sb * 4, 0, bar);
             }
             __syncwarp();
             if (nbytes) bulk_g2s(dst, src, nbytes, bar);
         }
     };
 
+    // Weights are constant inputs: their first stages stream while the preceding kernel in the
+    // stream finishes. x (and, per stage, its x tiles) is read only after that kernel is done.
+    pdl_launch_dependents();
     bool ok = true;
-    if (p.xres && nmine > 0 && lane == 0) {   // this warp's x slice, all tokens, once
-        mbar_arrive_expect_tx(xbar, p.x_tx);
-        tma_load_3d(xreg, &xmap, 0, kb0 * 4, 0, xbar);
+    if constexpr (XRES) {
+        for (int s = 0; s < D && s < total; ++s) issue(s, s);
+        pdl_wait();
+        if (nmine > 0 && lane == 0) {   // this warp's x slice, all tokens, once
+            mbar_arrive_expect_tx(xbar, p.x_tx);
+            tma_load_3d(xreg, &xmap, 0, kb0 * 4, 0, xbar);
+        }
+        if (nmine > 0) ok = mbar_wait(xbar, 0);
+        if constexpr (PERM) {   // [x0 x1 x2 x3] -> [x0 x2 x1 x3] inside every 16-byte chunk
+            for (uint32_t q = lane; q < p.x_tx / 16u; q += 32) {
+                const uint4 v = lds128(xreg + 16u * q);
+                sts128(xreg + 16u * q, make_uint4(prmt(v.x, v.y, 0x5410u), prmt(v.x, v.y, 0x7632u),
+                                                  prmt(v.z, v.w, 0x5410u), prmt(v.z, v.w, 0x7632u)));
+            }
+            __syncwarp();
+        }
+    } else {
+        pdl_wait();
+        for (int s = 0; s < D && s < total; ++s) issue(s, s);
     }
-    for (int s = 0; s < D && s < total; ++s) issue(s, s);
-    if (p.xres && nmine > 0) ok = mbar_wait(xbar, 0);
+    
 
     const uint32_t tok = static_cast<uint32_t>(min(g, p.M - 1));
-    const uint32_t xrows = p.xres ? 4u * p.kw : 4u * S;   // x rows per token in its tile
+    const uint32_t xrows = XRES ? 4u * p.kw : 4u * S;   // x rows per token in its tile
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     int u = 0;
     for (int t = 0; t < ntiles; ++t) {
@@ -480,10 +503,10 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ CU
             if (ok && !mbar_wait(bar0 + 8 * s, (u / D) & 1)) ok = false;
             if (ok) {
                 const uint32_t wst = wslot(s);
-                const uint32_t xst = p.xres ? xreg : xslot(s);
+                const uint32_t xst = XRES ? xreg : xslot(s);
                 const int sb0 = kb0 + si * S;
                 const int ns = min(S, kb1 - sb0);
-                const uint32_t xsb0 = p.xres ? static_cast<uint32_t>(si * S) : 0u;   // x superblock index base
+                const uint32_t xsb0 = XRES ? static_cast<uint32_t>(si * S) : 0u;   // x superblock index base
                 uint32_t base_a = wst + g * p.row_pitch, base_b = wst + (g + 8) * p.row_pitch;
                 if constexpr (!TMA) {   // block data starts (o & 15) bytes into the row's window
                     base_a += (static_cast<uint32_t>(ra * p.nsb + sb0) * static_cast<uint32_t>(BB)) & 15u;
@@ -492,8 +515,8 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ CU
                 for (int j = 0; j < ns; ++j) {
                     const uint32_t blk_a = base_a + j * BB, blk_b = base_b + j * BB;
                     const uint32_t r0 = tok * xrows + 4u * (xsb0 + j);   // x row of segment 0
-                    if constexpr (TYPE == 12 || TYPE == 13) superblock_kq<TYPE>(blk_a, blk_b, xrow(xst, r0 + c), c, acc);
-                    else if constexpr (TYPE == 14) superblock_q6(blk_a, blk_b, xst, r0, c, acc);
+                    if constexpr (TYPE == 12 || TYPE == 13) superblock_kq<TYPE, PERM>(blk_a, blk_b, xrow(xst, r0 + c), c, acc);
+                    else if constexpr (TYPE == 14) superblock_q6<PERM>(blk_a, blk_b, xst, r0, c, acc);
                     else superblock_iq4(blk_a, blk_b, xrow(xst, r0 + c), c, acc);
                 }
             }
@@ -600,33 +623,35 @@ GemvPlan make_plan(int type, int64_t N, int64_t K, int M, int num_sms) {
     return pl;
 }
 
-template <int TYPE, bool TMA>
+template <int TYPE, bool TMA, bool XRES>
 cudaError_t launch_t(const CUtensorMap &wm, const CUtensorMap &xm, const GemvArgs &a, int grid, int threads,
-                     size_t smem, cudaStream_t st) {
+                     size_t smem, bool pdl, cudaStream_t st) {
+    auto kern = gemv_kernel<TYPE, TMA, XRES>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_kernel<TYPE, TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             227 * 1024);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    gemv_kernel<TYPE, TMA><<<grid, threads, smem, st>>>(wm, xm, a);
-    return cudaGetLastError();
+    void *args[] = {const_cast<CUtensorMap *>(&wm), const_cast<CUtensorMap *>(&xm), const_cast<GemvArgs *>(&a)};
+    return launch_pdl(reinterpret_cast<const void *>(kern), dim3(grid), dim3(threads), smem, st, pdl, args);
 }
 
 template <int TYPE>
-cudaError_t launch_type(bool tma, const CUtensorMap &wm, const CUtensorMap &xm, const GemvArgs &a, int grid,
-                        int threads, size_t smem, cudaStream_t st) {
-    return tma ? launch_t<TYPE, true>(wm, xm, a, grid, threads, smem, st)
-               : launch_t<TYPE, false>(wm, xm, a, grid, threads, smem, st);
+cudaError_t launch_type(bool tma, bool xres, const CUtensorMap &wm, const CUtensorMap &xm, const GemvArgs &a,
+                        int grid, int threads, size_t smem, bool pdl, cudaStream_t st) {
+    if (tma) return xres ? launch_t<TYPE, true, true>(wm, xm, a, grid, threads, smem, pdl, st)
+                         : launch_t<TYPE, true, false>(wm, xm, a, grid, threads, smem, pdl, st);
+    return xres ? launch_t<TYPE, false, true>(wm, xm, a, grid, threads, smem, pdl, st)
+                : launch_t<TYPE, false, false>(wm, xm, a, grid, threads, smem, pdl, st);
 }
 
 }  // namespace
 
 cudaError_t gemv_launch(int type, const uint8_t *W, const __half *x, float *y, int64_t N, int64_t K, int M,
-                        unsigned *status, int num_sms, cudaStream_t stream) {
+                        unsigned *status, int num_sms, bool pdl, cudaStream_t stream) {
     const int bb = block_bytes_of(type);
     if (bb < 0 || M < 1 || M > kGemvMaxM) return cudaErrorInvalidValue;
     GemvPlan pl = make_plan(type, N, K, M, num_sms);
@@ -651,10 +676,10 @@ cudaError_t gemv_launch(int type, const uint8_t *W, const __half *x, float *y, i
     }
     const int threads = 32 * pl.warps;
     switch (type) {
-    case 12: return launch_type<12>(pl.tma, wm, xm, pl.a, pl.grid, threads, pl.smem, stream);
-    case 13: return launch_type<13>(pl.tma, wm, xm, pl.a, pl.grid, threads, pl.smem, stream);
-    case 14: return launch_type<14>(pl.tma, wm, xm, pl.a, pl.grid, threads, pl.smem, stream);
-    case 23: return launch_type<23>(pl.tma, wm, xm, pl.a, pl.grid, threads, pl.smem, stream);
+    case 12: return launch_type<12>(pl.tma, pl.a.xres != 0, wm, xm, pl.a, pl.grid, threads, pl.smem, pdl, stream);
+    case 13: return launch_type<13>(pl.tma, pl.a.xres != 0, wm, xm, pl.a, pl.grid, threads, pl.smem, pdl, stream);
+    case 14: return launch_type<14>(pl.tma, pl.a.xres != 0, wm, xm, pl.a, pl.grid, threads, pl.smem, pdl, stream);
+    case 23: return launch_type<23>(pl.tma, pl.a.xres != 0, wm, xm, pl.a, pl.grid, threads, pl.smem, pdl, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -16,16 +16,18 @@ int block_bytes_of(int type);
 
 constexpr int kGemvMaxM = 8;
 
-// y[M <= 8, N] = x . dequant(W)^T, one launch.
+// y[M <= 8, N] = x . dequant(W)^T, one launch. With `pdl` the kernel may start (and stream
+// its constant weights) while the preceding kernel in the stream finishes; it reads x and
+// writes y only after that kernel has completed.
 cudaError_t gemv_launch(int type, const uint8_t *W, const __half *x, float *y, int64_t N, int64_t K, int M,
-                        unsigned *status, int num_sms, cudaStream_t stream);
+                        unsigned *status, int num_sms, bool pdl, cudaStream_t stream);
 
 // ---------------------------------------------------------------- prefill GEMM (gemm_tc.cu)
 
 // Launches the tcgen05 kernel for any M >= 1. Returns cudaErrorNotSupported when the shape
 // cannot be handled (the caller maps it to QL_ERR_UNSUPPORTED).
 cudaError_t gemm_launch(int type, const uint8_t *W, const __half *x, float *y, int64_t N, int64_t K, int64_t M,
-                        unsigned *status, int num_sms, cudaStream_t stream);
+                        unsigned *status, int num_sms, bool pdl, cudaStream_t stream);
 int gemm_launch_count(int type, int64_t N, int64_t K, int64_t M);
 
 // ---------------------------------------------------------------- tensor maps (tmap.cu)
@@ -37,5 +39,8 @@ bool encode_tmap_2d(void *tmap_out, int dtype /* CUtensorMapDataType */, const v
 bool encode_tmap_3d(void *tmap_out, int dtype, const void *base, uint64_t dim0, uint64_t dim1, uint64_t dim2,
                     uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1, uint32_t box2,
                     bool swizzle128);
+
+// Launch `func` with its argument pointers, optionally as a programmatic dependent launch.
+cudaError_t launch_pdl(const void *func, dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl, void **args);
 
 }  // namespace ql

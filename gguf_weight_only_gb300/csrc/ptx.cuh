@@ -23,9 +23,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // Device-side status bits (OR-ed into the word the host passes to every kernel).
 enum : uint32_t { kStatusTimeout = 1u };
 
-// A bounded wait gives up after this much wall time; every wait in these kernels covers
-// work that completes in microseconds.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 
 // ---------------------------------------------------------------- mbarrier
 
@@ -65,16 +62,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that may suspend the thread for up to `ns` nanoseconds while the phase is not
+// complete (the thread resumes as soon as it completes).
+__device__ __forceinline__ bool mbar_try_wait_for(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+// SM-local cycle budget of a bounded wait (about 2 s at the GB300 SM clock).
+constexpr long long kWaitLimitCycles = 4000000000ll;
+
 // Wait for the phase with the given parity to complete. Returns false (and leaves the
-// barrier alone) if it has not completed within kWaitLimitNs.
+// barrier alone) if it has not completed within kWaitLimitCycles.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    const long long t0 = clock64();
+    while (!mbar_try_wait_for(bar, parity, 100000u)) {
+        if (clock64() - t0 > kWaitLimitCycles) return false;
     }
+    return true;
 }
 
 // ---------------------------------------------------------------- bulk copies (TMA engine)
@@ -110,6 +123,15 @@ __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Let the next kernel in the stream be scheduled as SM resources free up.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Block until the preceding kernel in the stream has completed and its writes are visible.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- shared memory loads
 
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
@@ -126,6 +148,9 @@ __device__ __forceinline__ uint32_t lds32(uint32_t a) {
     uint32_t v;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
     return v;
+}
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 __device__ __forceinline__ uint32_t lds16(uint32_t a) {
     uint16_t v;

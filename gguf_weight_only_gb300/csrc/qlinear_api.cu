@@ -1,6 +1,7 @@
 // qlinear_api.cu -- the C ABI declared in include/qlinear.h: argument validation, per-device
 // state, and dispatch on M between the decode GEMV and the tcgen05 prefill GEMM.
 #include <cstdint>
+#include <cstdlib>
 #include <mutex>
 
 #include "kernels.h"
@@ -15,6 +16,7 @@ struct DeviceState {
     bool ready = false;
     int status = QL_OK;       // QL_OK or the error of the failed initialisation
     int num_sms = 0;
+    bool pdl = true;          // programmatic dependent launch (QL_PDL=0 disables)
     unsigned *status_word = nullptr;
 };
 
@@ -50,6 +52,8 @@ int device_state(DeviceState **out) {
             if ((e = cudaGetSymbolAddress(&p, g_status_word)) != cudaSuccess) return cuda_fail(e);
             s.status_word = static_cast<unsigned *>(p);
             s.num_sms = sms;
+            const char *env = std::getenv("QL_PDL");
+            s.pdl = !(env && env[0] == '0');
             s.status = QL_OK;
         }
         s.ready = true;
@@ -79,7 +83,7 @@ int run_gemv(const DeviceState &s, int type, const void *W, int64_t N, int64_t K
         const int mg = static_cast<int>(M - m0 < ql::kGemvMaxM ? M - m0 : ql::kGemvMaxM);
         cudaError_t e = ql::gemv_launch(type, static_cast<const uint8_t *>(W),
                                         static_cast<const __half *>(x) + m0 * K, y + m0 * N, N, K, mg,
-                                        s.status_word, s.num_sms, st);
+                                        s.status_word, s.num_sms, s.pdl, st);
         if (e != cudaSuccess) return cuda_fail(e);
     }
     return QL_OK;
@@ -94,7 +98,7 @@ int run(Path path, int type, const void *W, int64_t N, int64_t K, const void *x,
     if (path == Path::Gemv || (path == Path::Auto && M <= ql::kGemvMaxM))
         return run_gemv(*s, type, W, N, K, x, M, y, st);
     cudaError_t e = ql::gemm_launch(type, static_cast<const uint8_t *>(W), static_cast<const __half *>(x), y, N, K, M,
-                                    s->status_word, s->num_sms, st);
+                                    s->status_word, s->num_sms, s->pdl, st);
     if (e == cudaErrorNotSupported) return QL_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return cuda_fail(e);
     return QL_OK;

@@ -1,5 +1,5 @@
-// tmap.cu -- host-side encoding of TMA tensor maps through the driver entry point
-// (no link-time dependency on libcuda).
+// tmap.cu -- host-side helpers: encoding of TMA tensor maps through the driver entry point
+// (no link-time dependency on libcuda) and kernel launches with programmatic dependent launch.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -68,6 +68,24 @@ bool encode_tmap_3d(void *tmap_out, int dtype, const void *base, uint64_t dim0, 
                            swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+}  // namespace ql
+
+namespace ql {
+
+cudaError_t launch_pdl(const void *func, dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl, void **args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelExC(&cfg, func, args);
 }
 
 }  // namespace ql

@@ -3,15 +3,18 @@
 //
 // Tiling ("swap AB"): a CTA owns 128 weight rows (the MMA's M side, one TMEM lane per row)
 // and a tile of n_tile tokens (the MMA's N side, 32..256). The fp32 accumulator lives in
-// TMEM columns [0, n_tile). K is walked in chunks of 64 (four MMAs of K = 16).
+// TMEM columns [0, n_tile). K is walked superblock by superblock (256 k = 16 MMAs of K = 16);
+// every hand-off between roles is per superblock, because on this part the issuing thread's
+// fixed cost per wait/fence/commit round (several hundred cycles) is far above the cost of
+// one MMA issue (about 50 cycles) and would otherwise starve the tensor pipe at small N.
 //
 // Warp roles (352 threads):
 //   warps 0-7  dequantisers: warp w serves TMEM lane quarter w % 4 (rows 32(w%4)..+31, one
 //              thread per row) and half w / 4 of every 64-wide chunk. Each thread decodes its
-//              row's 32 weights of the chunk from the staged superblock into fp16 and writes
-//              them with tcgen05.st into a TMEM A-operand ring (8 chunks x 32 columns); the
-//              MMA reads A straight from TMEM, so dequantised weights never touch shared
-//              memory. After the K loop the same warps drain the accumulator (tcgen05.ld) to y.
+//              row's 4 x 32 weights of a superblock from the staged block into fp16 and writes
+//              them with tcgen05.st into a TMEM A-operand ring (2 or 3 superblock slots of 128
+//              columns); the MMA reads A straight from TMEM, so dequantised weights never touch
+//              shared memory. After the K loop the same warps drain the accumulator to y.
 //   warp 8     weight producer: one 2-D TMA tensor copy per stage (S superblocks of the 128
 //              rows) into a shared-memory ring when rows are 16-byte multiples, else one bulk
 //              copy per row over the aligned window around the row's span.
@@ -32,8 +35,8 @@ namespace {
 
 constexpr int kRows = 128;          // weight rows per CTA (MMA M)
 constexpr int kChunkK = 64;         // k per pipeline chunk
-constexpr int kAStages = 8;         // TMEM A ring depth (chunks): columns 256..511
-constexpr uint32_t kACol = 256;     // first TMEM column of the A ring
+constexpr int kMaxASlots = 3;       // TMEM A ring: superblock slots of 128 columns
+constexpr uint32_t kASlotCols = 128;
 constexpr int kDequantWarps = 8;
 constexpr int kThreads = 32 * 11;
 constexpr uint32_t kTmemCols = 512;
@@ -48,6 +51,8 @@ struct GemmArgs {
     uint32_t row_pitch;        // bytes per weight row in a weight stage
     int qstages, bstages;
     int xk;                    // 64-wide chunks per activation stage (1, 2 or 4)
+    int a_slots;               // TMEM A ring depth in superblocks (2 or 3)
+    uint32_t a_col;            // first TMEM column of the A ring (256 or 128)
     uint32_t q_stage_bytes, b_stage_bytes;   // b stage = xk boxes of n_tile x 128 bytes
     uint32_t q_off, bar_off;   // offsets from the 1024-aligned shared base
     int64_t total_bytes;
@@ -236,9 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bfull = [&](int s) { return bars + 8u * (2 * QS + s); };
     auto bempty = [&](int s) { return bars + 8u * (2 * QS + BS + s); };
     auto afull = [&](int s) { return bars + 8u * (2 * QS + 2 * BS + s); };
-    auto aempty = [&](int s) { return bars + 8u * (2 * QS + 2 * BS + kAStages + s); };
-    const uint32_t accfull = bars + 8u * (2 * QS + 2 * BS + 2 * kAStages);
-    const uint32_t misc_off = p.bar_off + 8u * (2 * QS + 2 * BS + 2 * kAStages + 1);
+    auto aempty = [&](int s) { return bars + 8u * (2 * QS + 2 * BS + kMaxASlots + s); };
+    const uint32_t accfull = bars + 8u * (2 * QS + 2 * BS + 2 * kMaxASlots);
+    const uint32_t misc_off = p.bar_off + 8u * (2 * QS + 2 * BS + 2 * kMaxASlots + 1);
+    const int AS = p.a_slots;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + misc_off);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + misc_off + 4);
 
@@ -255,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bfull(s), 1);
             mbar_init(bempty(s), 1);
         }
-        for (int s = 0; s < kAStages; ++s) {
+        for (int s = 0; s < kMaxASlots; ++s) {
             mbar_init(afull(s), kDequantWarps);
             mbar_init(aempty(s), 1);
         }
@@ -284,40 +290,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = min(n0 + r, p.N - 1);
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
         bool ok = true;
-        KqRow kr{};
-        uint32_t blk = 0;
-        for (int chunk = 0; chunk < nchunks && ok; ++chunk) {
-            const int sb = chunk >> 2, gg = chunk & 3;
+        for (int sb = 0; sb < p.nsb && ok; ++sb) {
             const int si = sb / p.S, j = sb - si * p.S;   // weight stage and superblock within it
             const int qs = si % QS;
-            if (gg == 0) {
-                if (j == 0) {
-                    ok = wait_or_abort(qfull(qs), (si / QS) & 1, abort_flag, p.status);
-                    ok = __all_sync(0xFFFFFFFFu, ok);
-                    if (!ok) break;
-                }
-                blk = q_ring + qs * p.q_stage_bytes + r * p.row_pitch + j * p.bb;
-                if constexpr (!TMA)   // block data starts (o & 15) bytes into the row's window
-                    blk += (static_cast<uint32_t>(row * p.nsb + si * p.S) * static_cast<uint32_t>(p.bb)) & 15u;
-                if constexpr (TYPE == 12 || TYPE == 13) kr = kq_row(blk, h);
+            if (j == 0) {
+                ok = wait_or_abort(qfull(qs), (si / QS) & 1, abort_flag, p.status);
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                if (!ok) break;
             }
-            const int sa = chunk % kAStages;
-            ok = wait_or_abort(aempty(sa), ((chunk / kAStages) & 1) ^ 1, abort_flag, p.status);
+            uint32_t blk = q_ring + qs * p.q_stage_bytes + r * p.row_pitch + j * p.bb;
+            if constexpr (!TMA)   // block data starts (o & 15) bytes into the row's window
+                blk += (static_cast<uint32_t>(row * p.nsb + si * p.S) * static_cast<uint32_t>(p.bb)) & 15u;
+            KqRow kr{};
+            if constexpr (TYPE == 12 || TYPE == 13) kr = kq_row(blk, h);
+            const int sa = sb % AS;
+            ok = wait_or_abort(aempty(sa), ((sb / AS) & 1) ^ 1, abort_flag, p.status);
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
             tc_fence_after();
-            uint32_t out[16];
-            if constexpr (TYPE == 12) kq_chunk<false>(blk, gg, h, kr, out);
-            else if constexpr (TYPE == 13) kq_chunk<true>(blk, gg, h, kr, out);
-            else if constexpr (TYPE == 14) q6_chunk(blk, gg, h, out);
-            else iq4_chunk(blk, gg, h, out);
-            tmem_st16(tmem + lane_base + kACol + sa * 32 + 16 * h, out);
+            const uint32_t acol = tmem + lane_base + p.a_col + sa * kASlotCols + 16 * h;
+#pragma unroll
+            for (int gg = 0; gg < 4; ++gg) {
+                uint32_t out[16];
+                if constexpr (TYPE == 12) kq_chunk<false>(blk, gg, h, kr, out);
+                else if constexpr (TYPE == 13) kq_chunk<true>(blk, gg, h, kr, out);
+                else if constexpr (TYPE == 14) q6_chunk(blk, gg, h, out);
+                else iq4_chunk(blk, gg, h, out);
+                tmem_st16(acol + 32 * gg, out);
+            }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(afull(sa));
-                if (gg == 3 && (j == p.S - 1 || sb == p.nsb - 1)) mbar_arrive(qempty(qs));
+                if (j == p.S - 1 || sb == p.nsb - 1) mbar_arrive(qempty(qs));
             }
         }
         // ---------------------------------------------------- epilogue: TMEM -> y
@@ -428,22 +434,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc = idesc_f16_f32(kRows, p.n_tile);
             bool ok = true;
             const uint32_t box_bytes = static_cast<uint32_t>(p.n_tile) * 128u;
-            for (int chunk = 0; chunk < nchunks; ++chunk) {
-                const int sa = chunk % kAStages;
-                const int xs = chunk / p.xk, xi = chunk - xs * p.xk, sbb = xs % BS;
-                if (!wait_or_abort(afull(sa), (chunk / kAStages) & 1, abort_flag, p.status) ||
-                    (xi == 0 && !wait_or_abort(bfull(sbb), (xs / BS) & 1, abort_flag, p.status))) {
+            for (int sb = 0; sb < p.nsb && ok; ++sb) {
+                const int sa = sb % AS;
+                if (!wait_or_abort(afull(sa), (sb / AS) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t bst = b_ring + sbb * p.b_stage_bytes + xi * box_bytes;
+                const uint32_t a0 = tmem + p.a_col + sa * kASlotCols;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    tc_mma_ts(tmem, tmem + kACol + sa * 32 + kk * 8, smem_desc_sw128(bst + 32 * kk), idesc,
-                              (chunk | kk) != 0);
-                tc_commit(aempty(sa));
-                if (xi == p.xk - 1 || chunk == nchunks - 1) tc_commit(bempty(sbb));
+                for (int gg = 0; gg < 4; ++gg) {
+                    const int chunk = 4 * sb + gg;
+                    const int xs = chunk / p.xk, xi = chunk - xs * p.xk, sbb = xs % BS;
+                    if (xi == 0) {
+                        if (!wait_or_abort(bfull(sbb), (xs / BS) & 1, abort_flag, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                    const uint64_t bd = smem_desc_sw128(b_ring + sbb * p.b_stage_bytes + xi * box_bytes);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma_ts(tmem, a0 + 32 * gg + 8 * kk, bd + 2 * kk, idesc, (sb | gg | kk) != 0);
+                    if (xi == p.xk - 1 || chunk == nchunks - 1) tc_commit(bempty(sbb));
+                }
+                if (ok) tc_commit(aempty(sa));
             }
             tc_commit(accfull);   // also drains in-flight MMAs on the abort path
             if (!ok) (void)mbar_wait(accfull, 0);
@@ -469,7 +485,8 @@ int pick_n_tile(int64_t M) {
 }
 
 struct GemmPlan {
-    int n_tile, qstages, bstages, S, xk;
+    int n_tile, qstages, bstages, S, xk, a_slots;
+    uint32_t a_col;
     bool tma;
     uint32_t row_pitch, q_stage_bytes, b_stage_bytes, q_off, bar_off;
     size_t smem;
@@ -493,12 +510,15 @@ GemmPlan gemm_plan(int type, int bb, int64_t K, int64_t M) {
     // activation stages of about 32 KB: 1, 2 or 4 chunks of 64 columns
     pl.xk = pl.n_tile >= 256 ? 1 : pl.n_tile >= 128 ? 2 : 4;
     pl.b_stage_bytes = static_cast<uint32_t>(pl.n_tile) * 128u * pl.xk;
+    // TMEM: accumulator columns [0, n_tile), A ring after it in 128-column superblock slots
+    pl.a_col = pl.n_tile > 128 ? 256u : 128u;
+    pl.a_slots = static_cast<int>((kTmemCols - pl.a_col) / kASlotCols);
     const size_t limit = 227 * 1024 - 1024;
     for (int bs = 4; bs >= 2; --bs) {
         for (int qs = 8; qs >= 2; --qs) {
             const size_t q_off = static_cast<size_t>(bs) * pl.b_stage_bytes;
             const size_t bar_off = (q_off + static_cast<size_t>(qs) * pl.q_stage_bytes + 15) & ~size_t(15);
-            const size_t total = bar_off + 8 * (2 * qs + 2 * bs + 2 * kAStages + 1) + 16;
+            const size_t total = bar_off + 8 * (2 * qs + 2 * bs + 2 * kMaxASlots + 1) + 16;
             if (total <= limit) {
                 pl.bstages = bs;
                 pl.qstages = qs;
@@ -571,6 +591,8 @@ cudaError_t gemm_launch(int type, const uint8_t *W, const __half *x, float *y, i
     a.qstages = pl.qstages;
     a.bstages = pl.bstages;
     a.xk = pl.xk;
+    a.a_slots = pl.a_slots;
+    a.a_col = pl.a_col;
     a.q_stage_bytes = pl.q_stage_bytes;
     a.b_stage_bytes = pl.b_stage_bytes;
     a.q_off = pl.q_off;

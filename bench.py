@@ -9,6 +9,7 @@ step finds its weights in L2. The prefill figure (TFLOP/s of the Q4_K K=4096, N=
 GEMM) and the dominant kernels' roofline fractions ride along in the same JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --case TYPE,K,N,M [--steps K] [--warmup W]   # one layer shape, for profilers
 
 --impl reference times the fp64 CPU oracle on this machine's cores (a deliberately slow
 baseline) on a bounded sample of the same workload.
@@ -302,27 +303,31 @@ def run_ours(args, rank, world, local_rank):
 
 def cpu_baseline(budget_s=12.0):
     """The fp64 oracle (C, one POSIX thread per core) on a bounded sample of the decode
-    workload: the first rows of each layer shape, scaled to GB/s of that sample."""
+    workload: for each layer shape, its first rows (all of them when they fit), computed
+    repeatedly until about budget_s / 4 seconds have been spent; scaled to GB/s."""
     import oracle
     cores = len(os.sched_getaffinity(0))
-    total_bytes, total_s, rows_used = 0, 0.0, []
+    total_bytes, total_s, used = 0, 0.0, []
     for i, (K, N) in enumerate(DECODE_SHAPES):
         rows = max(cores, 64)
         W = synth.weights(DECODE_TYPE, rows, K, [11, i])
         x = synth.activations(DECODE_M, K, [12, i])
         t0 = time.perf_counter()
         oracle.qlinear(DECODE_TYPE, W, rows, K, x, n_threads=cores)
-        dt = time.perf_counter() - t0
-        # grow the sample to roughly budget/4 seconds per shape
-        rows = int(min(N, max(rows, rows * (budget_s / 4) / max(dt, 1e-6))))
+        dt = max(time.perf_counter() - t0, 1e-6)
+        rows = int(min(N, max(rows, rows * (budget_s / 4) / dt)))
         W = synth.weights(DECODE_TYPE, rows, K, [11, i])
-        t0 = time.perf_counter()
-        oracle.qlinear(DECODE_TYPE, W, rows, K, x, n_threads=cores)
-        total_s += time.perf_counter() - t0
-        total_bytes += alg_bytes(DECODE_TYPE, K, rows, DECODE_M)
-        rows_used.append(rows)
+        reps, spent = 0, 0.0
+        while spent < budget_s / 4 or reps == 0:
+            t0 = time.perf_counter()
+            oracle.qlinear(DECODE_TYPE, W, rows, K, x, n_threads=cores)
+            spent += time.perf_counter() - t0
+            reps += 1
+        total_s += spent
+        total_bytes += reps * alg_bytes(DECODE_TYPE, K, rows, DECODE_M)
+        used.append(f"{rows}x{reps}")
     return {"value": round(total_bytes / total_s / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"first {rows_used} rows of the four (K,N) decode shapes, M=1, fp64, {total_s:.1f} s"}
+            "sample": f"rows x passes per (K,N) decode shape: {used}, M=1, fp64, {total_s:.1f} s"}
 
 
 def run_reference(args):
@@ -364,6 +369,33 @@ def run_reference(args):
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_case(args):
+    """--case TYPE,K,N,M: W warm-up calls and then K calls of one layer shape through the
+    C ABI on fresh weights (no CUDA graph, no timing): the command profilers wrap."""
+    import torch
+    import gguf_weight_only_gb300 as ql
+    from gguf_weight_only_gb300 import build
+
+    t, K, N, M = (int(v) for v in args.case.split(","))
+    build.build()
+    lib = ql.lib()
+    dev = torch.device("cuda", 0)
+    W = torch.from_numpy(synth.weights(t, N, K, [7, t, K, N])).to(dev)
+    x = torch.from_numpy(synth.activations(M, K, [8, t, M])).to(dev)
+    y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    sh = torch.cuda.current_stream(dev).cuda_stream
+    for _ in range(args.warmup + args.steps):
+        rc = lib.qlinear(t, W.data_ptr(), N, K, x.data_ptr(), M, y.data_ptr(), sh)
+        if rc != 0:
+            raise RuntimeError(f"qlinear failed: {ql.strerror(rc)}")
+    torch.cuda.synchronize(dev)
+    st = ql.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st}")
+    print(json.dumps({"case": [t, K, N, M], "launches": args.warmup + args.steps,
+                      "kernel_launches_per_call": lib.qlinear_launch_count(t, N, K, M)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -371,8 +403,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--case", default=None, help="TYPE,K,N,M: run one layer shape (for profilers)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.case:
+        run_case(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

@@ -290,21 +290,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = min(n0 + r, p.N - 1);
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
         bool ok = true;
+        // ring positions as counters (no division on the critical path): weight stage qs with
+        // phase qph and superblock j within it; TMEM A slot sa with phase aph
+        int qs = 0, j = 0, sa = 0;
+        uint32_t qph = 0, aph = 0;
         for (int sb = 0; sb < p.nsb && ok; ++sb) {
-            const int si = sb / p.S, j = sb - si * p.S;   // weight stage and superblock within it
-            const int qs = si % QS;
             if (j == 0) {
-                ok = wait_or_abort(qfull(qs), (si / QS) & 1, abort_flag, p.status);
+                ok = wait_or_abort(qfull(qs), qph, abort_flag, p.status);
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) break;
             }
             uint32_t blk = q_ring + qs * p.q_stage_bytes + r * p.row_pitch + j * p.bb;
             if constexpr (!TMA)   // block data starts (o & 15) bytes into the row's window
-                blk += (static_cast<uint32_t>(row * p.nsb + si * p.S) * static_cast<uint32_t>(p.bb)) & 15u;
+                blk += (static_cast<uint32_t>(row * p.nsb + sb - j) * static_cast<uint32_t>(p.bb)) & 15u;
             KqRow kr{};
             if constexpr (TYPE == 12 || TYPE == 13) kr = kq_row(blk, h);
-            const int sa = sb % AS;
-            ok = wait_or_abort(aempty(sa), ((sb / AS) & 1) ^ 1, abort_flag, p.status);
+            ok = wait_or_abort(aempty(sa), aph ^ 1u, abort_flag, p.status);
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
             tc_fence_after();
@@ -324,6 +325,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 mbar_arrive(afull(sa));
                 if (j == p.S - 1 || sb == p.nsb - 1) mbar_arrive(qempty(qs));
+            }
+            if (++sa == AS) {
+                sa = 0;
+                aph ^= 1u;
+            }
+            if (++j == p.S) {
+                j = 0;
+                if (++qs == QS) {
+                    qs = 0;
+                    qph ^= 1u;
+                }
             }
         }
         // ---------------------------------------------------- epilogue: TMEM -> y
@@ -348,10 +360,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 8) {
         // ---------------------------------------------------- weight producer
         const int nstages = (p.nsb + p.S - 1) / p.S;
-        int issued = 0;
+        int issued = 0, s = 0;
+        uint32_t ph = 0;
         for (int si = 0; si < nstages; ++si) {
-            const int s = si % QS;
-            if (!wait_or_abort(qempty(s), ((si / QS) & 1) ^ 1, abort_flag, p.status)) break;
+            if (!wait_or_abort(qempty(s), ph ^ 1u, abort_flag, p.status)) break;
             fence_proxy_async_smem();
             const uint32_t st = q_ring + s * p.q_stage_bytes;
             if constexpr (TMA) {
@@ -403,6 +415,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (nb[i]) bulk_g2s(dst[i], src[i], nb[i], qfull(s));
             }
             issued = si + 1;
+            if (++s == QS) {
+                s = 0;
+                ph ^= 1u;
+            }
         }
         if (*abort_flag) {   // let issued copies land before the CTA's shared memory is released
             for (int si = max(0, issued - QS); si < issued; ++si) (void)mbar_wait(qfull(si % QS), (si / QS) & 1);
@@ -414,15 +430,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             int issued = 0;
             const int nx = (nchunks + p.xk - 1) / p.xk;
             const uint32_t box_bytes = static_cast<uint32_t>(p.n_tile) * 128u;
+            int s = 0;
+            uint32_t ph = 0;
             for (int xs = 0; xs < nx; ++xs) {
-                const int s = xs % BS;
-                if (!wait_or_abort(bempty(s), ((xs / BS) & 1) ^ 1, abort_flag, p.status)) break;
+                if (!wait_or_abort(bempty(s), ph ^ 1u, abort_flag, p.status)) break;
                 const int nb = min(p.xk, nchunks - xs * p.xk);
                 mbar_arrive_expect_tx(bfull(s), nb * box_bytes);
                 for (int i = 0; i < nb; ++i)
                     tma_load_2d(b_ring + s * p.b_stage_bytes + i * box_bytes, &xmap, (xs * p.xk + i) * kChunkK, t0,
                                 bfull(s));
                 issued = xs + 1;
+                if (++s == BS) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
             if (*abort_flag) {
                 for (int c = max(0, issued - BS); c < issued; ++c) (void)mbar_wait(bfull(c % BS), (c / BS) & 1);
@@ -434,9 +455,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc = idesc_f16_f32(kRows, p.n_tile);
             bool ok = true;
             const uint32_t box_bytes = static_cast<uint32_t>(p.n_tile) * 128u;
+            int sa = 0, xi = 0, sbb = 0;   // A slot, chunk within the x stage, x stage
+            uint32_t aph = 0, bph = 0;
             for (int sb = 0; sb < p.nsb && ok; ++sb) {
-                const int sa = sb % AS;
-                if (!wait_or_abort(afull(sa), (sb / AS) & 1, abort_flag, p.status)) {
+                if (!wait_or_abort(afull(sa), aph, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
@@ -444,10 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t a0 = tmem + p.a_col + sa * kASlotCols;
 #pragma unroll
                 for (int gg = 0; gg < 4; ++gg) {
-                    const int chunk = 4 * sb + gg;
-                    const int xs = chunk / p.xk, xi = chunk - xs * p.xk, sbb = xs % BS;
                     if (xi == 0) {
-                        if (!wait_or_abort(bfull(sbb), (xs / BS) & 1, abort_flag, p.status)) {
+                        if (!wait_or_abort(bfull(sbb), bph, abort_flag, p.status)) {
                             ok = false;
                             break;
                         }
@@ -457,9 +477,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         tc_mma_ts(tmem, a0 + 32 * gg + 8 * kk, bd + 2 * kk, idesc, (sb | gg | kk) != 0);
-                    if (xi == p.xk - 1 || chunk == nchunks - 1) tc_commit(bempty(sbb));
+                    if (++xi == p.xk || 4 * sb + gg == nchunks - 1) {
+                        tc_commit(bempty(sbb));
+                        xi = 0;
+                        if (++sbb == BS) {
+                            sbb = 0;
+                            bph ^= 1u;
+                        }
+                    }
                 }
                 if (ok) tc_commit(aempty(sa));
+                if (++sa == AS) {
+                    sa = 0;
+                    aph ^= 1u;
+                }
             }
             tc_commit(accfull);   // also drains in-flight MMAs on the abort path
             if (!ok) (void)mbar_wait(accfull, 0);

@@ -417,8 +417,7 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ CU
     auto wslot = [&](int s) { return ring + s * p.slot_bytes + (XRES ? 0u : p.x_bytes); };
     auto xslot = [&](int s) { return ring + s * p.slot_bytes; };
 
-    auto issue = [&](int s, int u) {
-        const int t = u / nst, si = u - t * nst;
+    auto issue = [&](int s, int t, int si) {
         const int sb = kb0 + si * S;
         const int row0 = r_begin + 16 * t;
         const uint32_t bar = bar0 + 8 * s;
@@ -469,8 +468,16 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ CU
     // stream finishes. x (and, per stage, its x tiles) is read only after that kernel is done.
     pdl_launch_dependents();
     bool ok = true;
+    int it = 0, isi = 0;   // next stage to issue: tile it, stage isi (counters, no division)
+    auto issue_next = [&](int s) {
+        issue(s, it, isi);
+        if (++isi == nst) {
+            isi = 0;
+            ++it;
+        }
+    };
     if constexpr (XRES) {
-        for (int s = 0; s < D && s < total; ++s) issue(s, s);
+        for (int s = 0; s < D && s < total; ++s) issue_next(s);
         pdl_wait();
         if (nmine > 0 && lane == 0) {   // this warp's x slice, all tokens, once
             mbar_arrive_expect_tx(xbar, p.x_tx);
@@ -487,20 +494,20 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ CU
         }
     } else {
         pdl_wait();
-        for (int s = 0; s < D && s < total; ++s) issue(s, s);
+        for (int s = 0; s < D && s < total; ++s) issue_next(s);
     }
     
 
     const uint32_t tok = static_cast<uint32_t>(min(g, p.M - 1));
     const uint32_t xrows = XRES ? 4u * p.kw : 4u * S;   // x rows per token in its tile
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    int u = 0;
+    int u = 0, s = 0;
+    uint32_t ph = 0;
     for (int t = 0; t < ntiles; ++t) {
         const int row0 = r_begin + 16 * t;
         const int ra = min(row0 + g, p.N - 1), rb = min(row0 + g + 8, p.N - 1);
         for (int si = 0; si < nst; ++si, ++u) {
-            const int s = u % D;
-            if (ok && !mbar_wait(bar0 + 8 * s, (u / D) & 1)) ok = false;
+            if (ok && !mbar_wait(bar0 + 8 * s, ph)) ok = false;
             if (ok) {
                 const uint32_t wst = wslot(s);
                 const uint32_t xst = XRES ? xreg : xslot(s);
@@ -523,7 +530,11 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ CU
             __syncwarp();
             if (ok && u + D < total) {
                 fence_proxy_async_smem();
-                issue(s, u + D);
+                issue_next(s);
+            }
+            if (++s == D) {
+                s = 0;
+                ph ^= 1u;
             }
         }
         // fixed-order reduction of the warps' 16 x 8 tiles of this row tile

@@ -78,6 +78,22 @@ def ncu_traffic(kernel_key):
     return None if v is None else float(v)
 
 
+def max_over_ranks(ms, world, dev=None):
+    """The slowest rank's time (all ranks must call it when world > 1)."""
+    if world <= 1:
+        return float(ms)
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(step_bytes, ms_step, world):
+    """Whole-job GB/s of `world` independent replicas, each moving step_bytes per step, timed
+    by the slowest rank's ms per step (weak scaling: per-GPU work is fixed)."""
+    return world * step_bytes / (ms_step * 1e-3) / 1e9
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons, sampled while the timed region runs."""
     Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -190,14 +206,10 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
-    ms_total = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(e0.elapsed_time(e1), world, dev)
     ms_step = ms_total / args.steps
     step_bytes = sum(alg_bytes(DECODE_TYPE, K, N, DECODE_M) for K, N in DECODE_SHAPES)
-    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    value = replica_throughput(step_bytes, ms_step, world)
     if ys[2].isnan().any():
         raise RuntimeError("NaN in output")
     del g

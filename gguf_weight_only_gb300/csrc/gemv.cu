@@ -80,6 +80,7 @@ struct KqConsts {
     uint32_t sc_lo, n1024_lo;   // (sc, sc), (-1024 sc, ...)      sub-block 2c   (low nibbles)
     uint32_t sc16_hi, n64_hi;   // (sc/16, ...), (-64 sc, ...)     sub-block 2c+1 (high nibbles)
     uint32_t m_lo, m_hi;        // (m, m) for the two sub-blocks
+    uint32_t m_pair;            // (m[2c], m[2c+1])
 };
 
 // Scales/mins of sub-blocks 2c and 2c+1 from the 12-byte field (header words y, z, w).
@@ -101,6 +102,7 @@ __device__ __forceinline__ KqConsts kq_consts(uint4 h, int c) {
     k.n64_hi = hmul2(sc1, kH2_m64);
     k.m_lo = hsub2(prmt(vm, 0x64646464u, 0x4040u), kH2_1024);
     k.m_hi = hsub2(prmt(vm, 0x64646464u, 0x4141u), kH2_1024);
+    k.m_pair = hsub2(prmt(vm, 0x64646464u, 0x4140u), kH2_1024);
     return k;
 }
 
@@ -161,8 +163,15 @@ __device__ __forceinline__ uint4 ldx(const XRow &x, uint32_t p) { return lds128(
 
 // Q4_K / Q5_K: lane (g, c) decodes 32-byte qs group c (sub-blocks 2c, 2c+1) of rows g, g+8.
 // xr = row of columns 64c .. 64c+63 of this superblock.
-template <int TYPE, bool PERM>
-__device__ __forceinline__ void superblock_kq(uint32_t blk_a, uint32_t blk_b, const XRow &xr, int c, float (&acc)[4]) {
+// The min term sum_j dmin m_j sum_{k in j} x_k factors through the sums of x over the eight
+// 32-wide sub-blocks (the group-sum idea). With XS those sums are staged (xsum = this
+// superblock's 32-byte record for this lane's token: pair c holds the hi and lo fp16 halves of
+// the sums of sub-blocks 2c, 2c+1) and ONE MMA with A = (m_2c, m_2c+1) in k-slots {2c, 2c+1}
+// and again in {2c+8, 2c+9} against B = (hi, lo) yields sum_j m_j (hi_j + lo_j). Without XS
+// every 16-wide piece runs its own MMA with A = m against x.
+template <int TYPE, bool PERM, bool XS>
+__device__ __forceinline__ void superblock_kq(uint32_t blk_a, uint32_t blk_b, const XRow &xr, int c, float (&acc)[4],
+                                              uint32_t xsum) {
     constexpr bool Q5 = (TYPE == 13);
     constexpr uint32_t QS = Q5 ? 48 : 16;
     const uint4 ha = lds128(blk_a), hb = lds128(blk_b);
@@ -191,9 +200,15 @@ __device__ __forceinline__ void superblock_kq(uint32_t blk_a, uint32_t blk_b, co
             const uint32_t y0 = v ? xh.z : xh.x, y1 = v ? xh.w : xh.y;
             mma16816(d1, la01, lb01, la23, lb23, x0, x1);
             mma16816(d1, ha01, hb01, ha23, hb23, y0, y1);
-            mma16816(d2, ka.m_lo, kb.m_lo, ka.m_lo, kb.m_lo, x0, x1);
-            mma16816(d2, ka.m_hi, kb.m_hi, ka.m_hi, kb.m_hi, y0, y1);
+            if constexpr (!XS) {
+                mma16816(d2, ka.m_lo, kb.m_lo, ka.m_lo, kb.m_lo, x0, x1);
+                mma16816(d2, ka.m_hi, kb.m_hi, ka.m_hi, kb.m_hi, y0, y1);
+            }
         }
+    }
+    if constexpr (XS) {
+        const uint2 sums = lds64(xsum + 8u * c);   // (hi_2c, hi_2c+1), (lo_2c, lo_2c+1)
+        mma16816(d2, ka.m_pair, kb.m_pair, ka.m_pair, kb.m_pair, sums.x, sums.y);
     }
     const float da = half_lo_to_float(ha.x), dma = half_hi_to_float(ha.x);
     const float db = half_lo_to_float(hb.x), dmb = half_hi_to_float(hb.x);
@@ -378,6 +393,7 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ CU
                                                       const __grid_constant__ CUtensorMap xmap, const GemvArgs p) {
     constexpr int BB = GemvFmt<TYPE>::BB;
     constexpr bool PERM = XRES && TYPE != 23;   // resident x is permuted once for the K-quant/Q6_K pairing
+    constexpr bool XSUM = XRES && (TYPE == 12 || TYPE == 13);   // staged sub-block sums of x (min term)
     extern __shared__ __align__(1024) uint8_t smem[];
     const int nwarps = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -390,6 +406,7 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ CU
     const uint32_t bar0 = base + 8u * warp * (D + 1);              // D ring barriers + 1 x barrier
     const uint32_t xbar = bar0 + 8u * D;
     const uint32_t xreg = base + p.x_offset + warp * p.x_warp_bytes;
+    const uint32_t xsum_base = xreg + p.x_tx;   // XSUM: [token][superblock of the slice] x 32 bytes
     const uint32_t ring = base + p.ring_offset + warp * D * p.slot_bytes;
 
     const int G = gridDim.x, b = blockIdx.x;
@@ -492,6 +509,27 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ CU
             }
             __syncwarp();
         }
+        if constexpr (XSUM) {   // sums of x over each 32-wide sub-block of the slice, fp16 hi + lo
+            const int per_tok = p.kw * 8;
+            for (int q = lane; q < p.M * per_tok; q += 32) {
+                const int tk = q / per_tok, rem = q - tk * per_tok, sbw = rem >> 3, j = rem & 7;
+                const XRow xr = xrow(xreg, static_cast<uint32_t>(tk * 4 * p.kw + 4 * sbw + (j >> 1)));
+                float sum = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 v = ldx(xr, static_cast<uint32_t>(4 * (j & 1) + i));
+                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sum += half_lo_to_float(w4[e]) + half_hi_to_float(w4[e]);
+                }
+                const __half hi = __float2half_rn(sum);
+                const __half lo = __float2half_rn(sum - __half2float(hi));
+                __half *rec = reinterpret_cast<__half *>(gbase + (xsum_base - base) + (tk * p.kw + sbw) * 32 + 8 * (j >> 1));
+                rec[j & 1] = hi;
+                rec[2 + (j & 1)] = lo;
+            }
+            __syncwarp();
+        }
     } else {
         pdl_wait();
         for (int s = 0; s < D && s < total; ++s) issue_next(s);
@@ -522,7 +560,9 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ CU
                 for (int j = 0; j < ns; ++j) {
                     const uint32_t blk_a = base_a + j * BB, blk_b = base_b + j * BB;
                     const uint32_t r0 = tok * xrows + 4u * (xsb0 + j);   // x row of segment 0
-                    if constexpr (TYPE == 12 || TYPE == 13) superblock_kq<TYPE, PERM>(blk_a, blk_b, xrow(xst, r0 + c), c, acc);
+                    if constexpr (TYPE == 12 || TYPE == 13)
+                        superblock_kq<TYPE, PERM, XSUM>(blk_a, blk_b, xrow(xst, r0 + c), c, acc,
+                                                        xsum_base + (tok * p.kw + xsb0 + j) * 32u);
                     else if constexpr (TYPE == 14) superblock_q6<PERM>(blk_a, blk_b, xst, r0, c, acc);
                     else superblock_iq4(blk_a, blk_b, xrow(xst, r0 + c), c, acc);
                 }
@@ -598,7 +638,8 @@ GemvPlan make_plan(int type, int64_t N, int64_t K, int M, int num_sms) {
         o.w_bytes = 16 * o.row_pitch;
         o.x_tx = static_cast<uint32_t>(M * (xres ? kw : S) * 512);
         o.x_bytes = xres ? 0u : o.x_tx;
-        o.x_warp_bytes = xres ? ((o.x_tx + 1023u) & ~1023u) : 0u;
+        const uint32_t xsum_bytes = (type == 12 || type == 13) ? static_cast<uint32_t>(M * kw * 32) : 0u;
+        o.x_warp_bytes = xres ? ((o.x_tx + xsum_bytes + 1023u) & ~1023u) : 0u;
         o.slot_bytes = (o.x_bytes + o.w_bytes + 1023u) & ~1023u;
         o.xres = xres ? 1 : 0;
         const uint32_t bars = static_cast<uint32_t>((w * (D + 1) * 8 + 1023) & ~1023);

@@ -293,14 +293,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ring positions as counters (no division on the critical path): weight stage qs with
         // phase qph and superblock j within it; TMEM A slot sa with phase aph
         int qs = 0, j = 0, sa = 0;
-        uint32_t qph = 0, aph = 0;
+        uint32_t qph = 0, aph = 0, stage = 0;
         for (int sb = 0; sb < p.nsb && ok; ++sb) {
             if (j == 0) {
                 ok = wait_or_abort(qfull(qs), qph, abort_flag, p.status);
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) break;
+                stage = q_ring + qs * p.q_stage_bytes;
             }
-            uint32_t blk = q_ring + qs * p.q_stage_bytes + r * p.row_pitch + j * p.bb;
+            uint32_t blk = stage + r * p.row_pitch + j * p.bb;
             if constexpr (!TMA)   // block data starts (o & 15) bytes into the row's window
                 blk += (static_cast<uint32_t>(row * p.nsb + sb - j) * static_cast<uint32_t>(p.bb)) & 15u;
             KqRow kr{};

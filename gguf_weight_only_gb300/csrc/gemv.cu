@@ -37,22 +37,33 @@ namespace {
 
 template <int TYPE>
 struct GemvFmt;
+// BB: bytes per superblock. MAXW: most warps per CTA (the decoders want about 128 registers
+// per thread: 16 warps fill the register file; fewer registers cost more than more warps gain).
 template <>
 struct GemvFmt<12> {   // Q4_K
-    static constexpr int BB = 144;
+    static constexpr int BB = 144, MAXW = 16;
 };
 template <>
 struct GemvFmt<13> {   // Q5_K
-    static constexpr int BB = 176;
+    static constexpr int BB = 176, MAXW = 16;
 };
 template <>
 struct GemvFmt<14> {   // Q6_K
-    static constexpr int BB = 210;
+    static constexpr int BB = 210, MAXW = 16;
 };
 template <>
 struct GemvFmt<23> {   // IQ4_XS
-    static constexpr int BB = 136;
+    static constexpr int BB = 136, MAXW = 16;
 };
+
+int gemv_max_warps(int type) {
+    switch (type) {
+    case 12: return GemvFmt<12>::MAXW;
+    case 13: return GemvFmt<13>::MAXW;
+    case 14: return GemvFmt<14>::MAXW;
+    default: return GemvFmt<23>::MAXW;
+    }
+}
 
 struct GemvArgs {
     const uint8_t *W;
@@ -62,6 +73,7 @@ struct GemvArgs {
     int N, K, M, nsb;
     int S;                   // superblocks per stage
     int kw;                  // superblocks of the K slice each warp owns
+    int ks, tgc;             // warp = tile group * ks + K slice: ks K slices x tgc tile groups
     int stages;              // ring depth per warp
     int xres;                // 1: x slice resident per warp; 0: x travels with each stage
     uint32_t row_pitch;      // bytes between rows inside a stage
@@ -71,6 +83,7 @@ struct GemvArgs {
     uint32_t x_warp_bytes;   // resident x region per warp
     uint32_t slot_bytes;     // one ring slot, rounded to 1 KB
     uint32_t red_offset, x_offset, ring_offset;
+    int round_tiles;         // row tiles whose partials are reduced together (one barrier pair)
     int64_t total_bytes;     // bytes of W
 };
 
@@ -185,7 +198,7 @@ __device__ __forceinline__ void superblock_kq(uint32_t blk_a, uint32_t blk_b, co
         hb1 = lds128(blk_b + 32);
     }
     const KqConsts ka = kq_consts(ha, c), kb = kq_consts(hb, c);
-    float d1[4] = {0.f, 0.f, 0.f, 0.f}, d2[4] = {0.f, 0.f, 0.f, 0.f};
+    float d1[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f}, d2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int u = 0; u < 8; u += 2) {
         const uint4 xl = ldx(xr, u >> 1);         // columns 64c + 4u .. +7   (low nibbles)
@@ -198,8 +211,8 @@ __device__ __forceinline__ void superblock_kq(uint32_t blk_a, uint32_t blk_b, co
             kq_word<Q5, PERM>(word_of(qb0, qb1, uu), word_of(hb0, hb1, uu), c, kb, lb01, lb23, hb01, hb23);
             const uint32_t x0 = v ? xl.z : xl.x, x1 = v ? xl.w : xl.y;
             const uint32_t y0 = v ? xh.z : xh.x, y1 = v ? xh.w : xh.y;
-            mma16816(d1, la01, lb01, la23, lb23, x0, x1);
-            mma16816(d1, ha01, hb01, ha23, hb23, y0, y1);
+            mma16816(d1, la01, lb01, la23, lb23, x0, x1);   // two independent accumulator chains
+            mma16816(e1, ha01, hb01, ha23, hb23, y0, y1);
             if constexpr (!XS) {
                 mma16816(d2, ka.m_lo, kb.m_lo, ka.m_lo, kb.m_lo, x0, x1);
                 mma16816(d2, ka.m_hi, kb.m_hi, ka.m_hi, kb.m_hi, y0, y1);
@@ -212,10 +225,10 @@ __device__ __forceinline__ void superblock_kq(uint32_t blk_a, uint32_t blk_b, co
     }
     const float da = half_lo_to_float(ha.x), dma = half_hi_to_float(ha.x);
     const float db = half_lo_to_float(hb.x), dmb = half_hi_to_float(hb.x);
-    acc[0] += da * d1[0] - dma * d2[0];
-    acc[1] += da * d1[1] - dma * d2[1];
-    acc[2] += db * d1[2] - dmb * d2[2];
-    acc[3] += db * d1[3] - dmb * d2[3];
+    acc[0] += da * (d1[0] + e1[0]) - dma * d2[0];
+    acc[1] += da * (d1[1] + e1[1]) - dma * d2[1];
+    acc[2] += db * (d1[2] + e1[2]) - dmb * d2[2];
+    acc[3] += db * (d1[3] + e1[3]) - dmb * d2[3];
 }
 
 // 16 bytes at a 2-byte aligned shared address, read as aligned words and realigned.
@@ -277,7 +290,7 @@ __device__ __forceinline__ void superblock_q6(uint32_t blk_a, uint32_t blk_b, ui
     const uint32_t offA = 64 * h + 16 * e, offB = 64 * h + 32 + 16 * e, offH = 128 + 32 * h + 16 * e;
     const uint4 qaA = lds128_a2(blk_a + offA), qaB = lds128_a2(blk_a + offB), qaH = lds128_a2(blk_a + offH);
     const uint4 qbA = lds128_a2(blk_b + offA), qbB = lds128_a2(blk_b + offB), qbH = lds128_a2(blk_b + offH);
-    float d1[4] = {0.f, 0.f, 0.f, 0.f};
+    float d1[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
         // columns 128h + 32t + 16e + 4u: segment 2h + t/2, chunk 4(t%2) + 2e + u/2
@@ -291,14 +304,15 @@ __device__ __forceinline__ void superblock_q6(uint32_t blk_a, uint32_t blk_b, ui
                 uint32_t a01, a23, b01, b23;
                 q6_pairs<PERM>(word4((t & 1) ? qaB : qaA, uu), word4(qaH, uu), t, sca[t], a01, a23);
                 q6_pairs<PERM>(word4((t & 1) ? qbB : qbA, uu), word4(qbH, uu), t, scb[t], b01, b23);
-                mma16816(d1, a01, b01, a23, b23, v ? xv.z : xv.x, v ? xv.w : xv.y);
+                if (v) mma16816(e1, a01, b01, a23, b23, xv.z, xv.w);
+                else mma16816(d1, a01, b01, a23, b23, xv.x, xv.y);
             }
         }
     }
-    acc[0] += da * d1[0];
-    acc[1] += da * d1[1];
-    acc[2] += db * d1[2];
-    acc[3] += db * d1[3];
+    acc[0] += da * (d1[0] + e1[0]);
+    acc[1] += da * (d1[1] + e1[1]);
+    acc[2] += db * (d1[2] + e1[2]);
+    acc[3] += db * (d1[3] + e1[3]);
 }
 
 // IQ4_XS codebook (test/unit/test_llm_quant_cpu.py, test_unpack_lut_dot_uop) stored as
@@ -349,7 +363,7 @@ __device__ __forceinline__ void superblock_iq4(uint32_t blk_a, uint32_t blk_b, c
     float da, db;
     iq4_row_consts(blk_a, c, lsa, nba, da);
     iq4_row_consts(blk_b, c, lsb, nbb, db);
-    float d1[4] = {0.f, 0.f, 0.f, 0.f};
+    float d1[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
         const uint32_t qoff = 8 + 32 * c + 16 * j;
@@ -368,14 +382,14 @@ __device__ __forceinline__ void superblock_iq4(uint32_t blk_a, uint32_t blk_b, c
                 iq4_word(wa, lsa[j], nba[j], al01, al23, ah01, ah23);
                 iq4_word(wb, lsb[j], nbb[j], bl01, bl23, bh01, bh23);
                 mma16816(d1, al01, bl01, al23, bl23, v ? xl.z : xl.x, v ? xl.w : xl.y);
-                mma16816(d1, ah01, bh01, ah23, bh23, v ? xh.z : xh.x, v ? xh.w : xh.y);
+                mma16816(e1, ah01, bh01, ah23, bh23, v ? xh.z : xh.x, v ? xh.w : xh.y);
             }
         }
     }
-    acc[0] += da * d1[0];
-    acc[1] += da * d1[1];
-    acc[2] += db * d1[2];
-    acc[3] += db * d1[3];
+    acc[0] += da * (d1[0] + e1[0]);
+    acc[1] += da * (d1[1] + e1[1]);
+    acc[2] += db * (d1[2] + e1[2]);
+    acc[3] += db * (d1[3] + e1[3]);
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -389,20 +403,19 @@ __device__ __forceinline__ void superblock_iq4(uint32_t blk_a, uint32_t blk_b, c
 // 16 x 8 partial tiles are summed in fixed order through shared memory.
 
 template <int TYPE, bool TMA, bool XRES>
-__global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ CUtensorMap wmap,
+__global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const __grid_constant__ CUtensorMap wmap,
                                                       const __grid_constant__ CUtensorMap xmap, const GemvArgs p) {
     constexpr int BB = GemvFmt<TYPE>::BB;
     constexpr bool PERM = XRES && TYPE != 23;   // resident x is permuted once for the K-quant/Q6_K pairing
     constexpr bool XSUM = XRES && (TYPE == 12 || TYPE == 13);   // staged sub-block sums of x (min term)
     extern __shared__ __align__(1024) uint8_t smem[];
-    const int nwarps = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
     const int D = p.stages, S = p.S;
 
     const uint32_t base = (smem_u32(smem) + 1023u) & ~1023u;   // the launch adds 1 KB of slack
     uint8_t *const gbase = smem + (base - smem_u32(smem));
-    float *red = reinterpret_cast<float *>(gbase + p.red_offset);   // [2][nwarps][32][4]
+    float *red = reinterpret_cast<float *>(gbase + p.red_offset);   // [round tile][K slice][token][16 rows]
     const uint32_t bar0 = base + 8u * warp * (D + 1);              // D ring barriers + 1 x barrier
     const uint32_t xbar = bar0 + 8u * D;
     const uint32_t xreg = base + p.x_offset + warp * p.x_warp_bytes;
@@ -416,11 +429,15 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ CU
     const int r_begin = 16 * t_begin, r_end = min(p.N, 16 * t_end);
     const int ntiles = t_end - t_begin;
 
-    const int kb0 = warp * p.kw;
+    // warp = (tile group tg, K slice kidx): it owns superblocks [kb0, kb1) of the CTA's tiles
+    // tg, tg + tgc, tg + 2 tgc, ...
+    const int kidx = warp % p.ks, tg = warp / p.ks;
+    const int kb0 = kidx * p.kw;
     const int kb1 = min(kb0 + p.kw, p.nsb);
     const int nmine = max(kb1 - kb0, 0);
     const int nst = (nmine + S - 1) / S;   // stages per tile for this warp (0 for idle warps)
-    const int total = ntiles * nst;
+    const int mytiles = ntiles > tg ? (ntiles - tg + p.tgc - 1) / p.tgc : 0;
+    const int total = mytiles * nst;
 
     if (lane == 0) {
         for (int s = 0; s <= D; ++s) mbar_init(bar0 + 8 * s, 1);
@@ -485,9 +502,9 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ CU
     // stream finishes. x (and, per stage, its x tiles) is read only after that kernel is done.
     pdl_launch_dependents();
     bool ok = true;
-    int it = 0, isi = 0;   // next stage to issue: tile it, stage isi (counters, no division)
+    int it = 0, isi = 0;   // next stage to issue: my tile it, stage isi (counters, no division)
     auto issue_next = [&](int s) {
-        issue(s, it, isi);
+        issue(s, tg + it * p.tgc, isi);
         if (++isi == nst) {
             isi = 0;
             ++it;
@@ -501,32 +518,34 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ CU
             tma_load_3d(xreg, &xmap, 0, kb0 * 4, 0, xbar);
         }
         if (nmine > 0) ok = mbar_wait(xbar, 0);
-        if constexpr (PERM) {   // [x0 x1 x2 x3] -> [x0 x2 x1 x3] inside every 16-byte chunk
+        if constexpr (PERM) {
+            // One pass over the warp's x tile: [x0 x1 x2 x3] -> [x0 x2 x1 x3] inside every 16-byte
+            // chunk and, for the K-quants, the sums of x over each 32-wide sub-block. The tile is
+            // 128-byte rows r = token * 4 kw + 4 * superblock + segment with chunk c of a row
+            // stored at c ^ (r & 7); that swizzle keeps each aligned group of four chunks (one
+            // sub-block) together, so four neighbouring lanes hold one sub-block and two shuffles
+            // sum it. x_tx / 16 is a multiple of 32: every lane runs every pass.
             for (uint32_t q = lane; q < p.x_tx / 16u; q += 32) {
                 const uint4 v = lds128(xreg + 16u * q);
                 sts128(xreg + 16u * q, make_uint4(prmt(v.x, v.y, 0x5410u), prmt(v.x, v.y, 0x7632u),
                                                   prmt(v.z, v.w, 0x5410u), prmt(v.z, v.w, 0x7632u)));
-            }
-            __syncwarp();
-        }
-        if constexpr (XSUM) {   // sums of x over each 32-wide sub-block of the slice, fp16 hi + lo
-            const int per_tok = p.kw * 8;
-            for (int q = lane; q < p.M * per_tok; q += 32) {
-                const int tk = q / per_tok, rem = q - tk * per_tok, sbw = rem >> 3, j = rem & 7;
-                const XRow xr = xrow(xreg, static_cast<uint32_t>(tk * 4 * p.kw + 4 * sbw + (j >> 1)));
-                float sum = 0.f;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint4 v = ldx(xr, static_cast<uint32_t>(4 * (j & 1) + i));
-                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) sum += half_lo_to_float(w4[e]) + half_hi_to_float(w4[e]);
+                if constexpr (XSUM) {
+                    const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
+                    const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
+                    const float2 f2 = __half22float2(*reinterpret_cast<const __half2 *>(&v.z));
+                    const float2 f3 = __half22float2(*reinterpret_cast<const __half2 *>(&v.w));
+                    float sum = ((f0.x + f0.y) + (f1.x + f1.y)) + ((f2.x + f2.y) + (f3.x + f3.y));
+                    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+                    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+                    if ((q & 3u) == 0u) {
+                        const uint32_t r = q >> 3, half = ((q & 7u) ^ (r & 7u)) >> 2;   // sub-block 2 (r & 3) + half
+                        const __half hi = __float2half_rn(sum);
+                        const __half lo = __float2half_rn(sum - __half2float(hi));
+                        __half *rec = reinterpret_cast<__half *>(gbase + (xsum_base - base) + (r >> 2) * 32u + 8u * (r & 3u));
+                        rec[half] = hi;
+                        rec[2 + half] = lo;
+                    }
                 }
-                const __half hi = __float2half_rn(sum);
-                const __half lo = __float2half_rn(sum - __half2float(hi));
-                __half *rec = reinterpret_cast<__half *>(gbase + (xsum_base - base) + (tk * p.kw + sbw) * 32 + 8 * (j >> 1));
-                rec[j & 1] = hi;
-                rec[2 + (j & 1)] = lo;
             }
             __syncwarp();
         }
@@ -539,9 +558,12 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ CU
     const uint32_t tok = static_cast<uint32_t>(min(g, p.M - 1));
     const uint32_t xrows = XRES ? 4u * p.kw : 4u * S;   // x rows per token in its tile
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    int u = 0, s = 0;
+    int u = 0, s = 0, jt = 0;   // stage counter, ring slot, my tile counter
     uint32_t ph = 0;
-    for (int t = 0; t < ntiles; ++t) {
+    for (int round0 = 0; round0 < ntiles; round0 += p.round_tiles) {
+      const int rend = min(round0 + p.round_tiles, ntiles);
+      for (; tg + jt * p.tgc < rend; ++jt) {
+        const int t = tg + jt * p.tgc;
         const int row0 = r_begin + 16 * t;
         const int ra = min(row0 + g, p.N - 1), rb = min(row0 + g + 8, p.N - 1);
         for (int si = 0; si < nst; ++si, ++u) {
@@ -567,30 +589,41 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ CU
                     else superblock_iq4(blk_a, blk_b, xrow(xst, r0 + c), c, acc);
                 }
             }
+            // Refill the slot. Its previous contents were read by this warp's ordinary loads,
+            // all consumed above (and kept ahead of the copy issue by its memory clobber), so
+            // the write-after-read needs no proxy fence.
             __syncwarp();
-            if (ok && u + D < total) {
-                fence_proxy_async_smem();
-                issue_next(s);
-            }
+            if (ok && u + D < total) issue_next(s);
             if (++s == D) {
                 s = 0;
                 ph ^= 1u;
             }
         }
-        // fixed-order reduction of the warps' 16 x 8 tiles of this row tile
-        float *rt = red + (t & 1) * nwarps * 128;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) rt[(warp * 32 + lane) * 4 + i] = acc[i];
-        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-        __syncthreads();
-        for (int q = threadIdx.x; q < 16 * p.M; q += blockDim.x) {
-            const int row = q & 15, tk = q >> 4;
-            const int src_lane = (row & 7) * 4 + (tk >> 1);
-            const int slot = ((row >> 3) << 1) | (tk & 1);
-            float sum = 0.f;
-            for (int w = 0; w < nwarps; ++w) sum += rt[(w * 32 + src_lane) * 4 + slot];
-            if (row0 + row < r_end) p.y[static_cast<int64_t>(tk) * p.N + row0 + row] = sum;
+        // This warp's partial of tile t goes to its slot of the current round (tokens < M only);
+        // warps run on without waiting for each other.
+        float *pt = red + ((t - round0) * p.ks + kidx) * 16 * p.M;
+        if (2 * c < p.M) {
+            pt[2 * c * 16 + g] = acc[0];
+            pt[2 * c * 16 + g + 8] = acc[2];
         }
+        if (2 * c + 1 < p.M) {
+            pt[(2 * c + 1) * 16 + g] = acc[1];
+            pt[(2 * c + 1) * 16 + g + 8] = acc[3];
+        }
+        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+      }
+      // end of the round: each tile's partials summed over its K slices in fixed order
+      __syncthreads();
+      const int per_tile = 16 * p.M;
+      for (int q = threadIdx.x; q < (rend - round0) * per_tile; q += blockDim.x) {
+          const int tt = q / per_tile, rem = q - tt * per_tile;   // tile of the round, token * 16 + row
+          const float *src = red + tt * p.ks * per_tile + rem;
+          float sum = 0.f;
+          for (int kk = 0; kk < p.ks; ++kk) sum += src[kk * per_tile];
+          const int grow = r_begin + 16 * (round0 + tt) + (rem & 15);
+          if (grow < r_end) p.y[static_cast<int64_t>(rem >> 4) * p.N + grow] = sum;
+      }
+      if (rend < ntiles) __syncthreads();   // the next round reuses the slots
     }
     if (!ok) {
         if (lane == 0) atomicOr(p.status, kStatusTimeout);
@@ -625,12 +658,32 @@ GemvPlan make_plan(int type, int64_t N, int64_t K, int M, int num_sms) {
         if ((pitch / 16) % 2 == 0) pitch += 16;                         // odd multiple of 16
         return pitch;
     };
-    // K slice per warp: up to 16 warps, slices a multiple of s_mult superblocks
-    int w = std::max(1, std::min(16, nsb / s_mult));
-    int kw = (nsb + w - 1) / w;
-    kw = (kw + s_mult - 1) / s_mult * s_mult;
-    w = (nsb + kw - 1) / kw;
     const size_t limit = 227 * 1024;
+    // grid: one CTA per SM (persistent), each owning up to tmax 16-row tiles
+    const int64_t T = (N + 15) / 16;
+    pl.grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(num_sms, T)));
+    const int tmax = static_cast<int>((T + pl.grid - 1) / pl.grid);
+    // Up to maxw warps = ks K slices (of kw superblocks, a multiple of s_mult) x tgc tile groups.
+    // Candidates are ranked by the busiest warp's work, kw * ceil(tmax / tgc) superblocks,
+    // then by more warps, then by fewer tile groups (less duplicated x).
+    struct Cand { int kw, ks, tgc, cost; };
+    const int maxw = gemv_max_warps(type);
+    Cand cands[32 * 32];
+    int nc = 0;
+    for (int want = 1; want <= maxw; ++want) {
+        int kw_ = (nsb + want - 1) / want;
+        kw_ = (kw_ + s_mult - 1) / s_mult * s_mult;
+        const int ks_ = (nsb + kw_ - 1) / kw_;
+        if (ks_ != want) continue;   // same split as a smaller count
+        for (int tgc_ = 1; ks_ * tgc_ <= maxw && tgc_ <= tmax; ++tgc_)
+            cands[nc++] = Cand{kw_, ks_, tgc_, kw_ * ((tmax + tgc_ - 1) / tgc_)};
+    }
+    std::sort(cands, cands + nc, [](const Cand &x, const Cand &y) {
+        if (x.cost != y.cost) return x.cost < y.cost;
+        if (x.ks * x.tgc != y.ks * y.tgc) return x.ks * x.tgc > y.ks * y.tgc;
+        return x.tgc < y.tgc;
+    });
+    int kw = 0, ks = 0, tgc = 0, w = 0, round_tiles = 1;
     auto layout = [&](bool xres, int S, int D, GemvArgs &o) {
         o.S = S;
         o.stages = D;
@@ -640,22 +693,32 @@ GemvPlan make_plan(int type, int64_t N, int64_t K, int M, int num_sms) {
         o.x_bytes = xres ? 0u : o.x_tx;
         const uint32_t xsum_bytes = (type == 12 || type == 13) ? static_cast<uint32_t>(M * kw * 32) : 0u;
         o.x_warp_bytes = xres ? ((o.x_tx + xsum_bytes + 1023u) & ~1023u) : 0u;
-        o.slot_bytes = (o.x_bytes + o.w_bytes + 1023u) & ~1023u;
+        // a slot that also holds a 128-byte-swizzled x tile starts on 1 KB, weights alone on 128 B
+        o.slot_bytes = xres ? ((o.w_bytes + 127u) & ~127u) : ((o.x_bytes + o.w_bytes + 1023u) & ~1023u);
         o.xres = xres ? 1 : 0;
         const uint32_t bars = static_cast<uint32_t>((w * (D + 1) * 8 + 1023) & ~1023);
         o.red_offset = bars;
-        o.x_offset = (bars + static_cast<uint32_t>(2 * w * 128 * sizeof(float)) + 1023u) & ~1023u;
+        o.round_tiles = round_tiles;
+        o.x_offset = (bars + static_cast<uint32_t>(round_tiles * ks * 16 * M * sizeof(float)) + 1023u) & ~1023u;
         o.ring_offset = o.x_offset + w * o.x_warp_bytes;
         return static_cast<size_t>(1024) + o.ring_offset + static_cast<size_t>(w) * D * o.slot_bytes;
     };
     size_t smem = 0;
     bool found = false;
-    for (int xres = 1; xres >= 0 && !found; --xres) {
-        for (int S = std::min(kw, s_max); S >= s_mult && !found; S -= s_mult) {
-            const int nst = (kw + S - 1) / S;
-            for (int D = std::min(4, std::max(2, 2 * nst)); D >= 2 && !found; --D) {
-                smem = layout(xres == 1, S, D, a);
-                found = smem <= limit;
+    for (int ci = 0; ci < nc && !found; ++ci) {
+        kw = cands[ci].kw;
+        ks = cands[ci].ks;
+        tgc = cands[ci].tgc;
+        w = ks * tgc;
+        // partials of up to round_tiles tiles (16 KB of shared memory) are reduced per round
+        round_tiles = std::max(1, std::min(tmax, (16 * 1024) / (ks * 16 * M * 4)));
+        for (int xres = 1; xres >= 0 && !found; --xres) {
+            for (int S = std::min(kw, s_max); S >= s_mult && !found; S -= s_mult) {
+                const int nst = (kw + S - 1) / S;
+                for (int D = std::min(4, std::max(2, 2 * nst)); D >= 2 && !found; --D) {
+                    smem = layout(xres == 1, S, D, a);
+                    found = smem <= limit;
+                }
             }
         }
     }
@@ -668,9 +731,10 @@ GemvPlan make_plan(int type, int64_t N, int64_t K, int M, int num_sms) {
     a.M = M;
     a.nsb = nsb;
     a.kw = kw;
+    a.ks = ks;
+    a.tgc = tgc;
     a.total_bytes = static_cast<int64_t>(N) * row_bytes;
     pl.warps = w;
-    pl.grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(num_sms, (N + 15) / 16)));
     pl.smem = smem;
     return pl;
 }

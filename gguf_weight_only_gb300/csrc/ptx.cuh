@@ -133,30 +133,25 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---------------------------------------------------------------- shared memory loads
+// Loads are ordinary C++ reads of the dynamic shared-memory window (every extern __shared__
+// array starts at its base), addressed by 32-bit shared-space addresses. Unlike volatile
+// inline asm they can be scheduled freely among themselves and the arithmetic, while the
+// compiler still keeps them behind every wait and ahead of every copy issue or release
+// (all of which are asm with a "memory" clobber).
 
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-    return v;
+extern __shared__ __align__(16) uint8_t ql_dyn_smem[];
+
+template <typename T>
+__device__ __forceinline__ T lds_as(uint32_t a) {
+    return *reinterpret_cast<const T *>(ql_dyn_smem + (a - static_cast<uint32_t>(__cvta_generic_to_shared(ql_dyn_smem))));
 }
-__device__ __forceinline__ uint2 lds64(uint32_t a) {
-    uint2 v;
-    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
-    return v;
-}
-__device__ __forceinline__ uint32_t lds32(uint32_t a) {
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
-    return v;
-}
+__device__ __forceinline__ uint4 lds128(uint32_t a) { return lds_as<uint4>(a); }
+__device__ __forceinline__ uint2 lds64(uint32_t a) { return lds_as<uint2>(a); }
+__device__ __forceinline__ uint32_t lds32(uint32_t a) { return lds_as<uint32_t>(a); }
 __device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
     asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
-__device__ __forceinline__ uint32_t lds16(uint32_t a) {
-    uint16_t v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
-    return v;
-}
+__device__ __forceinline__ uint32_t lds16(uint32_t a) { return lds_as<uint16_t>(a); }
 
 // ---------------------------------------------------------------- integer / fp16x2 helpers
 
@@ -210,7 +205,7 @@ constexpr uint32_t kH2_m1152 = 0xE480E480u;     // (-1152, -1152)
 // D(16x8, f32) += A(16x16, f16, row) * B(16x8, f16, col)
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])

@@ -37,23 +37,24 @@ namespace {
 
 template <int TYPE>
 struct GemvFmt;
-// BB: bytes per superblock. MAXW: most warps per CTA (the decoders want about 128 registers
-// per thread: 16 warps fill the register file; fewer registers cost more than more warps gain).
+// BB: bytes per superblock. MAXW: most warps per CTA. The decoders want about 128 registers
+// per thread; measured on GB300, 8 warps per SM (each with more superblocks per visit and a
+// deeper share of shared memory) outrun 16, and capping registers to fit more warps loses.
 template <>
 struct GemvFmt<12> {   // Q4_K
-    static constexpr int BB = 144, MAXW = 16;
+    static constexpr int BB = 144, MAXW = 8;
 };
 template <>
 struct GemvFmt<13> {   // Q5_K
-    static constexpr int BB = 176, MAXW = 16;
+    static constexpr int BB = 176, MAXW = 8;
 };
 template <>
 struct GemvFmt<14> {   // Q6_K
-    static constexpr int BB = 210, MAXW = 16;
+    static constexpr int BB = 210, MAXW = 8;
 };
 template <>
 struct GemvFmt<23> {   // IQ4_XS
-    static constexpr int BB = 136, MAXW = 16;
+    static constexpr int BB = 136, MAXW = 8;
 };
 
 int gemv_max_warps(int type) {

@@ -23,6 +23,8 @@
 //   warp 10    TMEM allocator and the single MMA-issuing thread.
 // All hand-offs are mbarriers; every wait is bounded and an expired wait aborts the CTA
 // (status word set, TMEM freed).
+#include <algorithm>
+#include <climits>
 #include <cstdint>
 #include <cuda.h>
 
@@ -344,8 +346,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (ok) {
             tc_fence_after();
-            const int half = p.n_tile / 2;
-            for (int c0 = h * half; c0 < (h + 1) * half; c0 += 16) {
+            // 16-column groups of the accumulator: the first half of them to h = 0, the rest to h = 1
+            const int ng = p.n_tile / 16, g_mid = ng / 2;
+            for (int c0 = 16 * (h ? g_mid : 0); c0 < 16 * (h ? ng : g_mid); c0 += 16) {
                 uint32_t v[16];
                 tmem_ld16(tmem + lane_base + c0, v);
                 tmem_wait_ld();
@@ -510,10 +513,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 namespace {
 
-int pick_n_tile(int64_t M) {
-    if (M >= 256) return 256;
-    int n = static_cast<int>((M + 31) / 32) * 32;
-    return n < 32 ? 32 : n;
+// Token tile: a multiple of 16 in [32, 256] minimising the estimated makespan, i.e. waves of
+// CTAs (row tiles x token tiles over the SMs) times the per-superblock time of one CTA, which
+// is the larger of its MMA time (8 n cycles: 16 MMAs of 128 x n x 16) and the time of its
+// dequantisers (about 1200 cycles, independent of n).
+int pick_n_tile(int64_t M, int64_t N, int num_sms) {
+    const int64_t row_tiles = (N + kRows - 1) / kRows;
+    int best = 32;
+    int64_t best_cost = INT64_MAX;
+    for (int n = 32; n <= 256; n += 16) {
+        const int64_t ntok = (M + n - 1) / n;
+        if (n > 32 && (ntok - 1) * n >= M) continue;   // a smaller tile covers M as well
+        const int64_t waves = (row_tiles * ntok + num_sms - 1) / num_sms;
+        const int64_t cost = waves * std::max<int64_t>(8 * n, 1200);
+        if (cost < best_cost) {   // ties keep the smaller tile (less padding)
+            best = n;
+            best_cost = cost;
+        }
+    }
+    return best;
 }
 
 struct GemmPlan {
@@ -524,9 +542,9 @@ struct GemmPlan {
     size_t smem;
 };
 
-GemmPlan gemm_plan(int type, int bb, int64_t K, int64_t M) {
+GemmPlan gemm_plan(int type, int bb, int64_t N, int64_t K, int64_t M, int num_sms) {
     GemmPlan pl{};
-    pl.n_tile = pick_n_tile(M);
+    pl.n_tile = pick_n_tile(M, N, num_sms);
     const int64_t nsb = K / 256;
     pl.S = (bb % 16 == 0) ? 1 : ((2 * bb) % 16 == 0 && nsb % 2 == 0) ? 2 : 1;
     pl.tma = ((nsb * bb) % 16 == 0) && ((pl.S * bb) % 16 == 0) && type != 14;
@@ -593,10 +611,10 @@ cudaError_t launch_type(bool tma, const CUtensorMap &xmap, const CUtensorMap &wm
 int gemm_launch_count(int, int64_t, int64_t, int64_t) { return 1; }
 
 cudaError_t gemm_launch(int type, const uint8_t *W, const __half *x, float *y, int64_t N, int64_t K, int64_t M,
-                        unsigned *status, int, bool pdl, cudaStream_t stream) {
+                        unsigned *status, int num_sms, bool pdl, cudaStream_t stream) {
     const int bb = block_bytes_of(type);
     if (bb < 0) return cudaErrorInvalidValue;
-    const GemmPlan pl = gemm_plan(type, bb, K, M);
+    const GemmPlan pl = gemm_plan(type, bb, N, K, M, num_sms > 0 ? num_sms : 148);
     if (pl.n_tile == 0) return cudaErrorNotSupported;
     CUtensorMap xmap{}, wmap{};
     if (!encode_tmap_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, static_cast<uint64_t>(K), static_cast<uint64_t>(M),

@@ -56,12 +56,18 @@ def peaks():
 
 
 def kernel_source_hash():
+    """Hash of the CUDA sources with comments and blank lines removed (a comment edit does
+    not invalidate counters taken on the same code)."""
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gguf_weight_only_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode())
-            h.update(f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        lines = [re.sub(r"//.*", "", ln).rstrip() for ln in text.splitlines()]
+        h.update(name.encode())
+        h.update("\n".join(ln for ln in lines if ln.strip()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,23 +1,25 @@
 // gemv.cu -- decode-path quantized linear y[M<=8, N] = x[M, K] . dequant(W)[N, K]^T.
 //
 // Design (sm_103a):
-//  * One CTA per 16 weight rows (one MMA row tile). Its warps split K: warp w owns a
-//    contiguous range of superblocks and streams them through its own ring of shared-memory
-//    stages. A stage holds S superblocks of all 16 rows and is filled by ONE 2-D TMA tensor
-//    copy (rows whose byte length is a multiple of 16), else by one bulk copy per row over
-//    the 16-byte aligned window around the row's span. Copies complete on the stage's
-//    mbarrier, so HBM bytes in flight cost no registers, and every weight byte is read from
-//    HBM exactly once.
-//  * x for the warp's K range is staged once into shared memory through registers, in the
-//    order the MMA fragments want (see below), with 16 bytes of padding per 64 columns.
+//  * Persistent: one CTA per SM owns a contiguous run of 16-row tiles. Its warps are
+//    (K slice, tile group) pairs: warp (kidx, tg) streams the superblocks of K slice kidx of
+//    the CTA's tiles tg, tg + tgc, ... through its own ring of shared-memory stages. A stage
+//    holds S superblocks of 16 rows and is filled by ONE 2-D TMA tensor copy (rows whose
+//    byte length is a multiple of 16), else by one bulk copy per row over the 16-byte aligned
+//    window around the row's span. Copies complete on the stage's mbarrier, so HBM bytes in
+//    flight cost no registers, and every weight byte is read from HBM exactly once.
+//  * The warp's slice of x (all tokens) lands once by TMA and is permuted in place into the
+//    order the MMA fragments want (see below); for the K-quants the same pass stores the
+//    sum of x over every 32-wide sub-block (fp16 hi + lo).
 //  * Each lane decodes its share of a block in registers into fp16 pairs that are EXACT
 //    integers (sc*q for K-quants, sc*(q-32) for Q6_K, (ls-32)*codebook[q] for IQ4_XS,
 //    the last two rounded only beyond 2048) and feeds them to the legacy tensor core
 //    (mma.sync m16n8k16, fp32 accumulate) with the tokens on the MMA's n = 8 side. The fp32
-//    superblock scale d (and dmin) is applied to per-superblock fp32 partial sums; the K-quant
-//    min term dmin * sum_j m_j * sum(x over sub-block j) runs through a second MMA whose A
-//    operand is the 6-bit min, constant per sub-block.
-//  * Warps' partial tiles are reduced in fixed order through shared memory (deterministic).
+//    superblock scale d is applied to per-superblock fp32 partial sums; the K-quant min term
+//    dmin * sum_j m_j * sum(x over sub-block j) is one MMA per superblock against the staged
+//    sub-block sums.
+//  * Per-tile partials of the warps go to shared memory; after a round of tiles they are
+//    summed over the K slices in fixed order (deterministic).
 // MMA fragment ownership (m16n8k16): lane = 4*g + c holds rows g and g+8 of A and k-slots
 // {2c, 2c+1, 2c+8, 2c+9}. The contraction does not care which real k sits in which slot, so
 // each lane assigns the k's it decoded to its own slots and reads x for exactly those k's.

@@ -22,7 +22,8 @@ STATUS = {0: "QL_OK", -1: "QL_ERR_TYPE", -2: "QL_ERR_SHAPE", -3: "QL_ERR_NULL", 
 # Every function include/qlinear.h declares (the symbol-export test checks this list
 # against the header).
 EXPORTS = ("qlinear", "qlinear_gemv", "qlinear_gemm", "qlinear_block_bytes", "qlinear_gemv_max_m",
-           "qlinear_strerror", "qlinear_last_cuda_error", "qlinear_device_status", "qlinear_launch_count")
+           "qlinear_strerror", "qlinear_last_cuda_error", "qlinear_device_status", "qlinear_launch_count",
+           "qlinear_selftest_wait_timeout")
 
 _lib = None
 
@@ -57,6 +58,8 @@ def lib() -> ctypes.CDLL:
         l.qlinear_device_status.restype = ctypes.c_int
         l.qlinear_launch_count.argtypes = [ctypes.c_int, i64, i64, i64]
         l.qlinear_launch_count.restype = ctypes.c_int
+        l.qlinear_selftest_wait_timeout.argtypes = [vp]
+        l.qlinear_selftest_wait_timeout.restype = ctypes.c_int
         _lib = l
     return _lib
 
@@ -83,6 +86,14 @@ def gemv_max_m() -> int:
 
 def launch_count(ggml_type: int, N: int, K: int, M: int) -> int:
     return lib().qlinear_launch_count(int(ggml_type), int(N), int(K), int(M))
+
+
+def selftest_wait_timeout(stream=None) -> None:
+    """Enqueue the diagnostic kernel whose bounded wait runs out (about 2 s); the next
+    device_status() then reports QL_ERR_TIMEOUT. Exercises the failure path without a fault."""
+    rc = lib().qlinear_selftest_wait_timeout(_stream_handle(stream))
+    if rc != 0:
+        raise QLinearError(rc, f"qlinear_selftest_wait_timeout: {strerror(rc)}")
 
 
 def _stream_handle(stream) -> int:

@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "kernels.h"
+#include "ptx.cuh"
 #include "qlinear.h"
 
 namespace {
@@ -76,6 +77,18 @@ int validate(int type, const void *W, int64_t N, int64_t K, const void *x, int64
 
 enum class Path { Auto, Gemv, Gemm };
 
+// One thread waits, with the library's bounded wait, on a barrier phase that never
+// completes; when the wait runs out it records the timeout in the status word.
+__global__ void wait_timeout_selftest_kernel(unsigned *status) {
+    __shared__ __align__(8) unsigned long long bar;
+    const uint32_t b = ql::smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        ql::mbar_init(b, 1);
+        ql::fence_mbar_init();
+        if (!ql::mbar_wait(b, 0)) atomicOr(status, ql::kStatusTimeout);
+    }
+}
+
 int run_gemv(const DeviceState &s, int type, const void *W, int64_t N, int64_t K, const void *x, int64_t M, float *y,
              cudaStream_t st) {
     // tokens in groups of kGemvMaxM: one launch per group (the weights stream once per group)
@@ -146,6 +159,15 @@ const char *qlinear_strerror(int status) {
 }
 
 int qlinear_last_cuda_error(void) { return t_last_cuda_error; }
+
+int qlinear_selftest_wait_timeout(void *stream) {
+    DeviceState *s = nullptr;
+    int rc = device_state(&s);
+    if (rc != QL_OK) return rc;
+    wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(s->status_word);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? QL_OK : cuda_fail(e);
+}
 
 int qlinear_device_status(void *stream) {
     DeviceState *s = nullptr;

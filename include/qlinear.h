@@ -110,6 +110,14 @@ int qlinear_device_status(void *stream);
  * QL_ERR_* on invalid arguments. */
 int qlinear_launch_count(int type, int64_t N, int64_t K, int64_t M);
 
+/* Diagnostic of the failure path: enqueues on `stream` one small kernel whose bounded wait
+ * on a barrier that nothing completes runs out (after about 2 s) and sets the device status
+ * word, exactly as an expired pipeline wait in the layer's kernels would. No fault is raised
+ * and the context stays usable; the next qlinear_device_status() reports QL_ERR_TIMEOUT.
+ * Returns QL_OK once enqueued, else an error. (Not part of the method; it tests the
+ * library's own error reporting.) */
+int qlinear_selftest_wait_timeout(void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -92,8 +92,8 @@ __device__ __forceinline__ KqRow kq_row(uint32_t blk, int h) {
     return r;
 }
 
-template <bool Q5>
-__device__ __forceinline__ void kq_chunk(uint32_t blk, int gg, int h, const KqRow &r, uint32_t (&out)[16]) {
+template <bool Q5, int h>
+__device__ __forceinline__ void kq_chunk(uint32_t blk, int gg, const KqRow &r, uint32_t (&out)[16]) {
     constexpr uint32_t QS = Q5 ? 48 : 16;
     const uint4 q0 = lds128(blk + QS + 32 * gg), q1 = lds128(blk + QS + 32 * gg + 16);
     uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
@@ -146,7 +146,8 @@ __device__ __forceinline__ uint4 lds128_a2(uint32_t addr) {
 }
 
 // Q6_K chunk gg: half hf = gg / 2 of the block, quarter t = 2 (gg % 2) + h, l = 0..31.
-__device__ __forceinline__ void q6_chunk(uint32_t blk, int gg, int h, uint32_t (&out)[16]) {
+template <int h>
+__device__ __forceinline__ void q6_chunk(uint32_t blk, int gg, uint32_t (&out)[16]) {
     const int hf = gg >> 1, t = 2 * (gg & 1) + h;
     const uint32_t d = lds16(blk + 208);
     const uint32_t d2 = d | (d << 16);
@@ -187,7 +188,8 @@ __device__ __forceinline__ uint32_t iq4_lookup(uint32_t s) {
 }
 
 // IQ4_XS chunk gg, half h: sub-block j = 2gg + h, 16 qs bytes -> [low nibbles, high nibbles].
-__device__ __forceinline__ void iq4_chunk(uint32_t blk, int gg, int h, uint32_t (&out)[16]) {
+template <int h>
+__device__ __forceinline__ void iq4_chunk(uint32_t blk, int gg, uint32_t (&out)[16]) {
     const int j = 2 * gg + h;
     const uint2 hd = lds64(blk);
     const uint32_t ls = ((hd.y >> (4 * j)) & 15u) | (((hd.x >> (16 + 2 * j)) & 3u) << 4);
@@ -203,6 +205,20 @@ __device__ __forceinline__ void iq4_chunk(uint32_t blk, int gg, int h, uint32_t 
         out[2 * u + 1] = hmul2(hsub2(prmt(r23, 0x64646464u, 0x4240u), kH2_1152), dl);   // p+2, p+3
         out[8 + 2 * u] = hmul2(hsub2(prmt(r01, 0x64646464u, 0x4341u), kH2_1152), dl);   // p+16, p+17
         out[9 + 2 * u] = hmul2(hsub2(prmt(r23, 0x64646464u, 0x4341u), kH2_1152), dl);   // p+18, p+19
+    }
+}
+
+// The four chunks of one superblock, half h, into TMEM columns acol + 32 gg + [0, 16).
+template <int TYPE, int h>
+__device__ __forceinline__ void dequant_superblock(uint32_t blk, const KqRow &kr, uint32_t acol) {
+#pragma unroll
+    for (int gg = 0; gg < 4; ++gg) {
+        uint32_t out[16];
+        if constexpr (TYPE == 12) kq_chunk<false, h>(blk, gg, kr, out);
+        else if constexpr (TYPE == 13) kq_chunk<true, h>(blk, gg, kr, out);
+        else if constexpr (TYPE == 14) q6_chunk<h>(blk, gg, out);
+        else iq4_chunk<h>(blk, gg, out);
+        tmem_st16(acol + 32 * gg, out);
     }
 }
 
@@ -313,15 +329,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t acol = tmem + lane_base + p.a_col + sa * kASlotCols + 16 * h;
-#pragma unroll
-            for (int gg = 0; gg < 4; ++gg) {
-                uint32_t out[16];
-                if constexpr (TYPE == 12) kq_chunk<false>(blk, gg, h, kr, out);
-                else if constexpr (TYPE == 13) kq_chunk<true>(blk, gg, h, kr, out);
-                else if constexpr (TYPE == 14) q6_chunk(blk, gg, h, out);
-                else iq4_chunk(blk, gg, h, out);
-                tmem_st16(acol + 32 * gg, out);
-            }
+            // the chunk half is warp-uniform: branch once so each decoder is specialised for it
+            if (h == 0) dequant_superblock<TYPE, 0>(blk, kr, acol);
+            else dequant_superblock<TYPE, 1>(blk, kr, acol);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();

@@ -556,17 +556,8 @@ GemmPlan gemm_plan(int type, int bb, int64_t N, int64_t K, int64_t M, int num_sm
     GemmPlan pl{};
     pl.n_tile = pick_n_tile(M, N, num_sms);
     const int64_t nsb = K / 256;
-    pl.S = (bb % 16 == 0) ? 1 : ((2 * bb) % 16 == 0 && nsb % 2 == 0) ? 2 : 1;
-    pl.tma = ((nsb * bb) % 16 == 0) && ((pl.S * bb) % 16 == 0) && type != 14;
-    uint32_t pitch;
-    if (pl.tma) {
-        pitch = static_cast<uint32_t>(pl.S * bb);   // dense rows as the tensor copy lands them
-    } else {   // window of the span incl. misalignment, an odd multiple of 16 bytes
-        pitch = static_cast<uint32_t>((pl.S * bb + 30) & ~15);
-        if ((pitch / 16) % 2 == 0) pitch += 16;
-    }
-    pl.row_pitch = pitch;
-    pl.q_stage_bytes = kRows * pitch;
+    const int s_tma = (bb % 16 == 0) ? 1 : ((2 * bb) % 16 == 0 && nsb % 2 == 0) ? 2 : 1;
+    pl.tma = ((nsb * bb) % 16 == 0) && ((s_tma * bb) % 16 == 0) && type != 14;
     // activation stages of about 32 KB: 1, 2 or 4 chunks of 64 columns
     pl.xk = pl.n_tile >= 256 ? 1 : pl.n_tile >= 128 ? 2 : 4;
     pl.b_stage_bytes = static_cast<uint32_t>(pl.n_tile) * 128u * pl.xk;
@@ -574,18 +565,37 @@ GemmPlan gemm_plan(int type, int bb, int64_t N, int64_t K, int64_t M, int num_sm
     pl.a_col = pl.n_tile > 128 ? 256u : 128u;
     pl.a_slots = static_cast<int>((kTmemCols - pl.a_col) / kASlotCols);
     const size_t limit = 227 * 1024 - 1024;
-    for (int bs = 4; bs >= 2; --bs) {
-        for (int qs = 8; qs >= 2; --qs) {
-            const size_t q_off = static_cast<size_t>(bs) * pl.b_stage_bytes;
-            const size_t bar_off = (q_off + static_cast<size_t>(qs) * pl.q_stage_bytes + 15) & ~size_t(15);
-            const size_t total = bar_off + 8 * (2 * qs + 2 * bs + 2 * kMaxASlots + 1) + 16;
-            if (total <= limit) {
-                pl.bstages = bs;
-                pl.qstages = qs;
-                pl.q_off = static_cast<uint32_t>(q_off);
-                pl.bar_off = static_cast<uint32_t>(bar_off);
-                pl.smem = total + 1024;   // slack for 1024-byte alignment of the base
-                return pl;
+    // Superblocks per weight stage: fixed by the tensor copy's box for TMA types; for rows
+    // copied one bulk copy each, as many as fit (up to 4), since the copy engine's cost is
+    // per copy and a stage of S superblocks needs 128 copies.
+    const int s_cands[3] = {4, 2, 1};
+    for (int ci = 0; ci < 3; ++ci) {
+        const int S = pl.tma ? s_tma : s_cands[ci];
+        if (pl.tma && ci > 0) break;
+        uint32_t pitch;
+        if (pl.tma) {
+            pitch = static_cast<uint32_t>(S * bb);   // dense rows as the tensor copy lands them
+        } else {   // window of the span incl. misalignment, an odd multiple of 16 bytes
+            pitch = static_cast<uint32_t>((S * bb + 30) & ~15);
+            if ((pitch / 16) % 2 == 0) pitch += 16;
+        }
+        const uint32_t q_stage_bytes = kRows * pitch;
+        for (int bs = 4; bs >= 2; --bs) {
+            for (int qs = 8; qs >= 2; --qs) {
+                const size_t q_off = static_cast<size_t>(bs) * pl.b_stage_bytes;
+                const size_t bar_off = (q_off + static_cast<size_t>(qs) * q_stage_bytes + 15) & ~size_t(15);
+                const size_t total = bar_off + 8 * (2 * qs + 2 * bs + 2 * kMaxASlots + 1) + 16;
+                if (total <= limit) {
+                    pl.S = S;
+                    pl.row_pitch = pitch;
+                    pl.q_stage_bytes = q_stage_bytes;
+                    pl.bstages = bs;
+                    pl.qstages = qs;
+                    pl.q_off = static_cast<uint32_t>(q_off);
+                    pl.bar_off = static_cast<uint32_t>(bar_off);
+                    pl.smem = total + 1024;   // slack for 1024-byte alignment of the base
+                    return pl;
+                }
             }
         }
     }

@@ -582,6 +582,7 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
                     base_a += (static_cast<uint32_t>(ra * p.nsb + sb0) * static_cast<uint32_t>(BB)) & 15u;
                     base_b += (static_cast<uint32_t>(rb * p.nsb + sb0) * static_cast<uint32_t>(BB)) & 15u;
                 }
+#pragma unroll 2   // two superblocks' independent decode chains can interleave
                 for (int j = 0; j < ns; ++j) {
                     const uint32_t blk_a = base_a + j * BB, blk_b = base_b + j * BB;
                     const uint32_t r0 = tok * xrows + 4u * (xsb0 + j);   // x row of segment 0

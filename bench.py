@@ -366,7 +366,7 @@ def run_reference(args):
         dt = max(time.perf_counter() - t0, 1e-6)
         rows = int(max(cores, min(N, rows * (per_step_s / 4) / dt)))
         samples.append((K, rows, synth.weights(DECODE_TYPE, rows, K, [11, i]), x))
-    vals = []
+    vals, times = [], []
     for s in range(args.warmup + args.steps):
         t0 = time.perf_counter()
         nbytes = 0
@@ -376,10 +376,12 @@ def run_reference(args):
         dt = time.perf_counter() - t0
         if s >= args.warmup:
             vals.append(nbytes / dt / 1e9)
+            times.append(dt)
     v = float(np.median(vals))
     sample = f"first {[r for _, r, _, _ in samples]} rows of the four (K,N) decode shapes per step, M=1, fp64"
     return {"metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
-            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "warmup": args.warmup, "ms_per_step": round(float(np.median(times)) * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": {"workload": "Q4_K decode, 8B-class layer: M=1, (K,N) in (4096,4096),(4096,1024),(4096,12288),(12288,4096)",
                        "parallelism": "host cores"},

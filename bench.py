@@ -152,8 +152,8 @@ def run_ours(args, rank, world, local_rank):
     import gguf_weight_only_gb300 as ql
     from gguf_weight_only_gb300 import build
 
-    if rank == 0 or not os.path.exists(build.LIB):
-        build.build()
+    if rank == 0:
+        build.build()   # one build; the other ranks wait for it, then load the same library
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.set_device(local_rank)

@@ -10,6 +10,7 @@ GEMM) and the dominant kernels' roofline fractions ride along in the same JSON l
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
   python bench.py --case TYPE,K,N,M [--steps K] [--warmup W]   # one layer shape, for profilers
+  python bench.py --table                                        # every layer shape, timed alone
 
 --impl reference times the fp64 CPU oracle on this machine's cores (a deliberately slow
 baseline) on a bounded sample of the same workload.
@@ -222,34 +223,7 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- dominant decode kernel alone: largest shape, CUDA-event time per launch
     def time_kernel(t, K, N, M, path_fn, reps):
-        wb = N * (K // 256) * BB[t]
-        Pk = max(2, int(np.ceil(2.2 * l2 / wb)))
-        W0 = torch.from_numpy(synth.weights(t, N, K, [7, t, K, N])).to(dev)
-        Wk = [W0.clone() for _ in range(Pk)]
-        x = torch.from_numpy(synth.activations(M, K, [8, t, M])).to(dev)
-        y = torch.empty((M, N), dtype=torch.float32, device=dev)
-        with torch.cuda.stream(stream):
-            for i in range(3):
-                path_fn(t, Wk[i % Pk].data_ptr(), N, K, x.data_ptr(), M, y.data_ptr(), sh)
-        torch.cuda.synchronize(dev)
-        gk = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gk, stream=stream):
-            for i in range(reps):
-                path_fn(t, Wk[i % Pk].data_ptr(), N, K, x.data_ptr(), M, y.data_ptr(), sh)
-        with torch.cuda.stream(stream):
-            gk.replay()
-        torch.cuda.synchronize(dev)
-        best = []
-        for _ in range(3):
-            with torch.cuda.stream(stream):
-                e0.record(stream)
-                gk.replay()
-                e1.record(stream)
-            torch.cuda.synchronize(dev)
-            best.append(e0.elapsed_time(e1) / reps)
-        del gk, Wk
-        torch.cuda.empty_cache()
-        return float(np.median(best))
+        return time_shape(t, K, N, M, path_fn, reps, dev, stream, l2)
 
     Kd, Nd = DECODE_SHAPES[2]
     ms_dec = time_kernel(DECODE_TYPE, Kd, Nd, DECODE_M, lib.qlinear, 200)
@@ -315,6 +289,86 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and world == 1:
         result["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
     return result
+
+
+
+def time_shape(t, K, N, M, path_fn, reps, dev, stream, l2, replays=3):
+    """CUDA-event time (ms) of one launch of a layer shape: a CUDA graph of `reps` back-to-back
+    calls over rotated weight copies (more than 2.2x L2 in total, so weights come from HBM),
+    replayed `replays` times after one untimed replay; the median per-launch time."""
+    import torch
+    wb = N * (K // 256) * BB[t]
+    Pk = max(2, int(np.ceil(2.2 * l2 / wb)))
+    W0 = torch.from_numpy(synth.weights(t, N, K, [7, t, K, N])).to(dev)
+    Wk = [W0.clone() for _ in range(Pk)]
+    x = torch.from_numpy(synth.activations(M, K, [8, t, M])).to(dev)
+    y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    sh = stream.cuda_stream
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            path_fn(t, Wk[i % Pk].data_ptr(), N, K, x.data_ptr(), M, y.data_ptr(), sh)
+    torch.cuda.synchronize(dev)
+    gk = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gk, stream=stream):
+        for i in range(reps):
+            path_fn(t, Wk[i % Pk].data_ptr(), N, K, x.data_ptr(), M, y.data_ptr(), sh)
+    with torch.cuda.stream(stream):
+        gk.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for _ in range(replays):
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            gk.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(e0.elapsed_time(e1) / reps)
+    if y.isnan().any():
+        raise RuntimeError("NaN in output")
+    del gk, Wk
+    torch.cuda.empty_cache()
+    return float(np.median(times))
+
+
+# Every layer shape of the scope table: (type, K, N, M)
+TABLE_SHAPES = [
+    (12, 1024, 1024, 1),
+    (12, 4096, 4096, 1), (12, 4096, 1024, 1), (12, 4096, 12288, 1), (12, 12288, 4096, 1),
+    (12, 4096, 4096, 4), (12, 4096, 12288, 4), (12, 12288, 4096, 4),
+    (23, 5120, 5120, 1), (23, 5120, 17408, 1), (23, 17408, 5120, 1),
+    (13, 5120, 17408, 1), (14, 5120, 17408, 1),
+    (12, 4096, 12288, 32), (12, 4096, 12288, 128), (12, 4096, 12288, 512),
+    (13, 5120, 17408, 256), (14, 5120, 17408, 256),
+]
+TYPE_NAMES = {12: "Q4_K", 13: "Q5_K", 14: "Q6_K", 23: "IQ4_XS"}
+
+
+def run_table(args):
+    """--table: every layer shape of the scope table timed alone (time_shape, median of 5
+    replays), one JSON line per shape with GB/s, TFLOP/s and the fraction of the measured
+    peak that bounds it (HBM for M <= 64, the tensor pipe above)."""
+    import torch
+    import gguf_weight_only_gb300 as ql
+    from gguf_weight_only_gb300 import build
+
+    build.build()
+    lib = ql.lib()
+    dev = torch.device("cuda", 0)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    hbm, tf_burst, _, peak_kind = peaks()
+    stream = torch.cuda.Stream(device=dev)
+    for t, K, N, M in TABLE_SHAPES:
+        ms = time_shape(t, K, N, M, lib.qlinear, 200 if M <= 8 else 40, dev, stream, l2, replays=5)
+        gbs = alg_bytes(t, K, N, M) / (ms * 1e-3) / 1e9
+        tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        bound = "hbm" if M <= 64 else "tensor"
+        frac = gbs / hbm if bound == "hbm" else tf / tf_burst
+        print(json.dumps({"type": TYPE_NAMES[t], "K": K, "N": N, "M": M,
+                          "path": "gemv" if M <= lib.qlinear_gemv_max_m() else "gemm",
+                          "us": round(ms * 1e3, 2), "GBs": round(gbs, 1), "TFLOPs": round(tf, 1),
+                          "bound": bound, "frac": round(frac, 4), "peak_kind": peak_kind,
+                          "status": ql.device_status()}), flush=True)
 
 
 # ---------------------------------------------------------------------------- oracle on the CPU
@@ -424,10 +478,14 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--case", default=None, help="TYPE,K,N,M: run one layer shape (for profilers)")
+    ap.add_argument("--table", action="store_true", help="time every layer shape of the scope table")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.case:
         run_case(args)
+        return
+    if args.table:
+        run_table(args)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -331,6 +331,68 @@ def time_shape(t, K, N, M, path_fn, reps, dev, stream, l2, replays=3):
     return float(np.median(times))
 
 
+def time_multi(t, K, Ns, M, reps, dev, stream, l2, lib, fused=True, replays=5):
+    """As time_shape, for projections sharing x: one qlinear_multi call per repetition (fused)
+    or one qlinear call per projection (separate). Returns ms per repetition."""
+    import ctypes
+    import torch
+    wb = sum(N * (K // 256) * BB[t] for N in Ns)
+    Pk = max(2, int(np.ceil(2.2 * l2 / wb)))
+    W0 = [torch.from_numpy(synth.weights(t, N, K, [7, t, K, N, j])).to(dev) for j, N in enumerate(Ns)]
+    Wk = [[w.clone() for w in W0] for _ in range(Pk)]
+    x = torch.from_numpy(synth.activations(M, K, [8, t, M])).to(dev)
+    ys = [torch.empty((M, N), dtype=torch.float32, device=dev) for N in Ns]
+    sh = stream.cuda_stream
+    n = len(Ns)
+    n_arr = (ctypes.c_int64 * n)(*Ns)
+    y_arr = (ctypes.c_void_p * n)(*[y.data_ptr() for y in ys])
+    w_arrs = [(ctypes.c_void_p * n)(*[w.data_ptr() for w in Ws]) for Ws in Wk]
+
+    def call(i):
+        if fused:
+            rc = lib.qlinear_multi(t, n, w_arrs[i % Pk], n_arr, K, x.data_ptr(), M, y_arr, sh)
+            if rc != 0:
+                raise RuntimeError(f"qlinear_multi failed: {rc}")
+        else:
+            for j, N in enumerate(Ns):
+                rc = lib.qlinear(t, Wk[i % Pk][j].data_ptr(), N, K, x.data_ptr(), M, ys[j].data_ptr(), sh)
+                if rc != 0:
+                    raise RuntimeError(f"qlinear failed: {rc}")
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            call(i)
+    torch.cuda.synchronize(dev)
+    gk = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gk, stream=stream):
+        for i in range(reps):
+            call(i)
+    with torch.cuda.stream(stream):
+        gk.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for _ in range(replays):
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            gk.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(e0.elapsed_time(e1) / reps)
+    if any(y.isnan().any() for y in ys):
+        raise RuntimeError("NaN in output")
+    del gk, Wk
+    torch.cuda.empty_cache()
+    return float(np.median(times))
+
+
+# Projection sets sharing x (one qlinear_multi call each): name, type, K, (N_j), M
+TABLE_MULTI = [
+    ("8B Q/K/V", 12, 4096, (4096, 1024, 1024), 1),
+    ("8B gate/up", 12, 4096, (12288, 12288), 1),
+    ("27B Q/K/V", 23, 5120, (5120, 1024, 1024), 1),
+]
+
 # Every layer shape of the scope table: (type, K, N, M)
 TABLE_SHAPES = [
     (12, 1024, 1024, 1),
@@ -369,6 +431,15 @@ def run_table(args):
                           "us": round(ms * 1e3, 2), "GBs": round(gbs, 1), "TFLOPs": round(tf, 1),
                           "bound": bound, "frac": round(frac, 4), "peak_kind": peak_kind,
                           "status": ql.device_status()}), flush=True)
+    for name, t, K, Ns, M in TABLE_MULTI:
+        byts = sum(alg_bytes(t, K, N, M) for N in Ns) - 2 * M * K * (len(Ns) - 1)   # x read once
+        res = {}
+        for fused in (True, False):
+            ms = time_multi(t, K, Ns, M, 200, dev, stream, l2, lib, fused=fused)
+            res["fused" if fused else "separate"] = {"us": round(ms * 1e3, 2), "GBs": round(byts / (ms * 1e-3) / 1e9, 1),
+                                                     "frac": round(byts / (ms * 1e-3) / 1e9 / hbm, 4)}
+        print(json.dumps({"projections": name, "type": TYPE_NAMES[t], "K": K, "N": list(Ns), "M": M, **res,
+                          "peak_kind": peak_kind, "status": ql.device_status()}), flush=True)
 
 
 # ---------------------------------------------------------------------------- oracle on the CPU

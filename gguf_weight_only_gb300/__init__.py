@@ -23,7 +23,7 @@ STATUS = {0: "QL_OK", -1: "QL_ERR_TYPE", -2: "QL_ERR_SHAPE", -3: "QL_ERR_NULL", 
 # against the header).
 EXPORTS = ("qlinear", "qlinear_gemv", "qlinear_gemm", "qlinear_block_bytes", "qlinear_gemv_max_m",
            "qlinear_strerror", "qlinear_last_cuda_error", "qlinear_device_status", "qlinear_launch_count",
-           "qlinear_selftest_wait_timeout")
+           "qlinear_selftest_wait_timeout", "qlinear_multi", "qlinear_max_projections")
 
 _lib = None
 
@@ -60,6 +60,11 @@ def lib() -> ctypes.CDLL:
         l.qlinear_launch_count.restype = ctypes.c_int
         l.qlinear_selftest_wait_timeout.argtypes = [vp]
         l.qlinear_selftest_wait_timeout.restype = ctypes.c_int
+        l.qlinear_multi.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(vp), ctypes.POINTER(i64), i64, vp, i64,
+                                    ctypes.POINTER(vp), vp]
+        l.qlinear_multi.restype = ctypes.c_int
+        l.qlinear_max_projections.argtypes = []
+        l.qlinear_max_projections.restype = ctypes.c_int
         _lib = l
     return _lib
 
@@ -136,6 +141,44 @@ def qlinear(W, ggml_type: int, N: int, K: int, x, out=None, path: str = "auto", 
         raise ValueError("out must be a contiguous float32 CUDA tensor with M*N elements")
     qlinear_raw(path, ggml_type, W.data_ptr(), N, K, x.data_ptr(), M, out.data_ptr(), _stream_handle(stream))
     return out
+
+
+def max_projections() -> int:
+    return lib().qlinear_max_projections()
+
+
+def qlinear_multi(Ws, ggml_type: int, Ns, K: int, x, outs=None, stream=None):
+    """[y_j] = [x . dequant(W_j)^T] for projections sharing x and K, in one decode launch
+    when M <= 8 (each W_j a uint8 CUDA tensor of Ns[j] rows; x float16 (M, K) or (K,))."""
+    import torch
+    Ws, Ns = list(Ws), [int(n) for n in Ns]
+    if len(Ws) != len(Ns):
+        raise ValueError("Ws and Ns differ in length")
+    if not (isinstance(x, torch.Tensor) and x.is_cuda and x.dtype == torch.float16):
+        raise TypeError("x must be a float16 CUDA tensor")
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    if x.dim() != 2 or x.shape[1] != K or not x.is_contiguous():
+        raise ValueError(f"x must be a contiguous (M, {K}) tensor")
+    M = x.shape[0]
+    bb = block_bytes(ggml_type)
+    for W, N in zip(Ws, Ns):
+        if not (isinstance(W, torch.Tensor) and W.is_cuda and W.dtype == torch.uint8 and W.is_contiguous()):
+            raise TypeError("each W must be a contiguous uint8 CUDA tensor")
+        if bb > 0 and W.numel() < N * (K // 256) * bb:
+            raise ValueError("a W holds fewer bytes than N*K/256 superblocks")
+    if outs is None:
+        outs = [torch.empty((M, N), dtype=torch.float32, device=x.device) for N in Ns]
+    elif len(outs) != len(Ns) or not all(o.is_cuda and o.dtype == torch.float32 and o.is_contiguous()
+                                         and o.numel() >= M * N for o, N in zip(outs, Ns)):
+        raise ValueError("outs must be contiguous float32 CUDA tensors of M*N[j] elements")
+    n = len(Ws)
+    w_arr = (ctypes.c_void_p * max(n, 1))(*[W.data_ptr() for W in Ws])
+    n_arr = (ctypes.c_int64 * max(n, 1))(*Ns)
+    y_arr = (ctypes.c_void_p * max(n, 1))(*[o.data_ptr() for o in outs])
+    _check(lib().qlinear_multi(int(ggml_type), n, w_arr, n_arr, int(K), x.data_ptr(), M, y_arr,
+                               _stream_handle(stream)), "qlinear_multi")
+    return outs
 
 
 def device_status(stream=None) -> int:

@@ -1,4 +1,5 @@
-// gemv.cu -- decode-path quantized linear y[M<=8, N] = x[M, K] . dequant(W)[N, K]^T.
+// gemv.cu -- decode-path quantized linear y[M<=8, N] = x[M, K] . dequant(W)[N, K]^T, for one
+// weight matrix or for up to four sharing x and K (projections; their row tiles form one list).
 //
 // Design (sm_103a):
 //  * Persistent: one CTA per SM owns a contiguous run of 16-row tiles. Its warps are
@@ -39,7 +40,7 @@ namespace {
 
 template <int TYPE>
 struct GemvFmt;
-// BB: bytes per superblock. MAXW: most warps per CTA. The decoders want about 128 registers
+// BB: bytes per superblock. MAXW: most warps per CTA. The decoders take 124 to 168 registers
 // per thread; measured on GB300, 8 warps per SM (each with more superblocks per visit and a
 // deeper share of shared memory) outrun 16, and capping registers to fit more warps loses.
 template <>
@@ -69,11 +70,17 @@ int gemv_max_warps(int type) {
 }
 
 struct GemvArgs {
-    const uint8_t *W;
+    // projections j < nproj share K and x: W[j] holds N[j] rows, y[j] is [M, N[j]], and
+    // projection j owns row tiles [tile0[j], tile0[j+1]) of the concatenated tile space
+    const uint8_t *W[kGemvMaxProj];
+    float *y[kGemvMaxProj];
+    int64_t total_bytes[kGemvMaxProj];   // bytes of W[j]
+    int N[kGemvMaxProj];
+    int tile0[kGemvMaxProj + 1];
+    int nproj;
     const __half *x;
-    float *y;
     unsigned *status;
-    int N, K, M, nsb;
+    int K, M, nsb;
     int S;                   // superblocks per stage
     int kw;                  // superblocks of the K slice each warp owns
     int ks, tgc;             // warp = tile group * ks + K slice: ks K slices x tgc tile groups
@@ -87,7 +94,11 @@ struct GemvArgs {
     uint32_t slot_bytes;     // one ring slot, rounded to 1 KB
     uint32_t red_offset, x_offset, ring_offset;
     int round_tiles;         // row tiles whose partials are reduced together (one barrier pair)
-    int64_t total_bytes;     // bytes of W
+};
+
+// Weight tensor maps, one per projection (unused entries stay zero).
+struct GemvMaps {
+    CUtensorMap m[kGemvMaxProj];
 };
 
 // ---------------------------------------------------------------- K-quant scale constants
@@ -397,17 +408,18 @@ __device__ __forceinline__ void superblock_iq4(uint32_t blk_a, uint32_t blk_b, c
 
 // ---------------------------------------------------------------- the kernel
 //
-// Persistent: CTA b owns a contiguous run of 16-row tiles (an equal share of the T = N/16
-// tiles, G = grid size, one CTA per SM) and walks them in order; warp w owns the
-// fixed K slice of superblocks [w kw, (w+1) kw) for every tile, so its slice of x is loaded
-// once (xres) or, when that does not fit, with each stage. Each warp streams its units
-// (tile, stage of S superblocks) through a ring of `stages` slots, issuing a slot's next
-// unit as soon as it has consumed it, across tile boundaries. After each tile the warps'
-// 16 x 8 partial tiles are summed in fixed order through shared memory.
+// Persistent: CTA b owns a contiguous run of 16-row tiles (an equal share of the T tiles of all
+// projections, G = grid size, one CTA per SM). Warp (kidx, tg) owns the fixed K slice of
+// superblocks [kidx kw, (kidx+1) kw) of the CTA's tiles tg, tg + tgc, ..., so its slice of x
+// is loaded once (xres) or, when that does not fit, with each stage. Each warp streams its
+// units (tile, stage of S superblocks) through a ring of `stages` slots, issuing a slot's
+// next unit as soon as it has consumed it, across tile boundaries. The warps' 16 x 8 partial
+// tiles go to shared memory; after each round of tiles they are summed in fixed order.
 
-template <int TYPE, bool TMA, bool XRES>
-__global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const __grid_constant__ CUtensorMap wmap,
-                                                      const __grid_constant__ CUtensorMap xmap, const GemvArgs p) {
+template <int TYPE, bool TMA, bool XRES, bool MULTI>
+__global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const __grid_constant__ GemvMaps wmaps,
+                                                      const __grid_constant__ CUtensorMap xmap,
+                                                      const __grid_constant__ GemvArgs p) {
     constexpr int BB = GemvFmt<TYPE>::BB;
     constexpr bool PERM = XRES && TYPE != 23;   // resident x is permuted once for the K-quant/Q6_K pairing
     constexpr bool XSUM = XRES && (TYPE == 12 || TYPE == 13);   // staged sub-block sums of x (min term)
@@ -426,11 +438,18 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
     const uint32_t ring = base + p.ring_offset + warp * D * p.slot_bytes;
 
     const int G = gridDim.x, b = blockIdx.x;
-    const int T = (p.N + 15) / 16;   // row tiles; CTA b owns tiles [T b / G, T (b+1) / G)
+    const int T = p.tile0[p.nproj];   // row tiles of all projections; CTA b owns [T b / G, T (b+1) / G)
     const int t_begin = static_cast<int>(static_cast<int64_t>(T) * b / G);
     const int t_end = static_cast<int>(static_cast<int64_t>(T) * (b + 1) / G);
-    const int r_begin = 16 * t_begin, r_end = min(p.N, 16 * t_end);
     const int ntiles = t_end - t_begin;
+    // CTA-local tile t -> its projection j and its first row within that projection
+    auto tile_rows = [&](int t, int &j) {
+        const int gt = t_begin + t;
+        j = 0;
+        if constexpr (!MULTI) return 16 * gt;   // one projection: the lookup cost 3-4% on GB300
+        while (j + 1 < p.nproj && gt >= p.tile0[j + 1]) ++j;
+        return 16 * (gt - p.tile0[j]);
+    };
 
     // warp = (tile group tg, K slice kidx): it owns superblocks [kb0, kb1) of the CTA's tiles
     // tg, tg + tgc, tg + 2 tgc, ...
@@ -446,7 +465,8 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
         for (int s = 0; s <= D; ++s) mbar_init(bar0 + 8 * s, 1);
         fence_mbar_init();
         prefetch_tmap(&xmap);
-        if constexpr (TMA) prefetch_tmap(&wmap);
+        if constexpr (TMA)
+            for (int j = 0; j < p.nproj; ++j) prefetch_tmap(&wmaps.m[j]);
     }
     __syncwarp();
 
@@ -456,13 +476,14 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
 
     auto issue = [&](int s, int t, int si) {
         const int sb = kb0 + si * S;
-        const int row0 = r_begin + 16 * t;
+        int j;
+        const int row0 = tile_rows(t, j);
         const uint32_t bar = bar0 + 8 * s;
         const uint32_t xtx = XRES ? 0u : p.x_tx;
         if constexpr (TMA) {
             if (lane == 0) {
                 mbar_arrive_expect_tx(bar, p.w_bytes + xtx);
-                tma_load_2d(wslot(s), &wmap, sb * (BB / 8), row0, bar);
+                tma_load_2d(wslot(s), &wmaps.m[j], sb * (BB / 8), row0, bar);
                 if (!XRES) tma_load_3d(xslot(s), &xmap, 0, sb * 4, 0, bar);
             }
         } else {
@@ -472,23 +493,24 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
             int tail_len = 0;
             uint32_t tail_off = 0;
             int64_t t16 = 0;
-            if (lane < 16 && row0 + lane < r_end) {
+            const uint8_t *const W = p.W[j];
+            if (lane < 16 && row0 + lane < p.N[j]) {
                 const int64_t o = (static_cast<int64_t>(row0 + lane) * p.nsb + sb) * BB;
                 const int64_t lo = o & ~int64_t(15);
                 int64_t hi = (o + static_cast<int64_t>(ns) * BB + 15) & ~int64_t(15);
-                t16 = p.total_bytes & ~int64_t(15);
+                t16 = p.total_bytes[j] & ~int64_t(15);
                 if (hi > t16) {   // the span ends in the last, partial 16 bytes of W
                     hi = t16;
                     tail_len = static_cast<int>(o + static_cast<int64_t>(ns) * BB - t16);
                     tail_off = static_cast<uint32_t>(t16 - lo);
                 }
-                src = p.W + lo;
+                src = W + lo;
                 dst = wslot(s) + lane * p.row_pitch;
                 nbytes = static_cast<uint32_t>(hi - lo);
             }
             if (tail_len > 0) {
                 uint8_t *gd = smem + (dst + tail_off - smem_u32(smem));
-                for (int i = 0; i < tail_len; ++i) gd[i] = __ldg(p.W + t16 + i);
+                for (int i = 0; i < tail_len; ++i) gd[i] = __ldg(W + t16 + i);
             }
             const uint32_t sum = __reduce_add_sync(0xFFFFFFFFu, nbytes);
             __syncwarp();
@@ -567,8 +589,9 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
       const int rend = min(round0 + p.round_tiles, ntiles);
       for (; tg + jt * p.tgc < rend; ++jt) {
         const int t = tg + jt * p.tgc;
-        const int row0 = r_begin + 16 * t;
-        const int ra = min(row0 + g, p.N - 1), rb = min(row0 + g + 8, p.N - 1);
+        int jp;
+        const int row0 = tile_rows(t, jp);
+        const int ra = min(row0 + g, p.N[jp] - 1), rb = min(row0 + g + 8, p.N[jp] - 1);
         for (int si = 0; si < nst; ++si, ++u) {
             if (ok && !mbar_wait(bar0 + 8 * s, ph)) ok = false;
             if (ok) {
@@ -624,8 +647,9 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
           const float *src = red + tt * p.ks * per_tile + rem;
           float sum = 0.f;
           for (int kk = 0; kk < p.ks; ++kk) sum += src[kk * per_tile];
-          const int grow = r_begin + 16 * (round0 + tt) + (rem & 15);
-          if (grow < r_end) p.y[static_cast<int64_t>(rem >> 4) * p.N + grow] = sum;
+          int jp;
+          const int row = tile_rows(round0 + tt, jp) + (rem & 15);
+          if (row < p.N[jp]) p.y[jp][static_cast<int64_t>(rem >> 4) * p.N[jp] + row] = sum;
       }
       if (rend < ntiles) __syncthreads();   // the next round reuses the slots
     }
@@ -645,7 +669,8 @@ struct GemvPlan {
     size_t smem;
 };
 
-GemvPlan make_plan(int type, int64_t N, int64_t K, int M, int num_sms) {
+// T: 16-row tiles over all projections.
+GemvPlan make_plan(int type, int64_t T, int64_t K, int M, int num_sms) {
     GemvPlan pl{};
     GemvArgs &a = pl.a;
     const int bb = block_bytes_of(type);
@@ -664,7 +689,6 @@ GemvPlan make_plan(int type, int64_t N, int64_t K, int M, int num_sms) {
     };
     const size_t limit = 227 * 1024;
     // grid: one CTA per SM (persistent), each owning up to tmax 16-row tiles
-    const int64_t T = (N + 15) / 16;
     pl.grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(num_sms, T)));
     const int tmax = static_cast<int>((T + pl.grid - 1) / pl.grid);
     // Up to maxw warps = ks K slices (of kw superblocks, a multiple of s_mult) x tgc tile groups.
@@ -730,14 +754,12 @@ GemvPlan make_plan(int type, int64_t N, int64_t K, int M, int num_sms) {
         pl.smem = SIZE_MAX;
         return pl;
     }
-    a.N = static_cast<int>(N);
     a.K = static_cast<int>(K);
     a.M = M;
     a.nsb = nsb;
     a.kw = kw;
     a.ks = ks;
     a.tgc = tgc;
-    a.total_bytes = static_cast<int64_t>(N) * row_bytes;
     pl.warps = w;
     // Ask for more than half of an SM's shared memory even when the plan needs less: the
     // partition assumes one CTA per SM, and two CTAs doubled up on one SM (which the block
@@ -747,10 +769,10 @@ GemvPlan make_plan(int type, int64_t N, int64_t K, int M, int num_sms) {
     return pl;
 }
 
-template <int TYPE, bool TMA, bool XRES>
-cudaError_t launch_t(const CUtensorMap &wm, const CUtensorMap &xm, const GemvArgs &a, int grid, int threads,
+template <int TYPE, bool TMA, bool XRES, bool MULTI>
+cudaError_t launch_t(const GemvMaps &wm, const CUtensorMap &xm, const GemvArgs &a, int grid, int threads,
                      size_t smem, bool pdl, cudaStream_t st) {
-    auto kern = gemv_kernel<TYPE, TMA, XRES>;
+    auto kern = gemv_kernel<TYPE, TMA, XRES, MULTI>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -759,32 +781,54 @@ cudaError_t launch_t(const CUtensorMap &wm, const CUtensorMap &xm, const GemvArg
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    void *args[] = {const_cast<CUtensorMap *>(&wm), const_cast<CUtensorMap *>(&xm), const_cast<GemvArgs *>(&a)};
+    void *args[] = {const_cast<GemvMaps *>(&wm), const_cast<CUtensorMap *>(&xm), const_cast<GemvArgs *>(&a)};
     return launch_pdl(reinterpret_cast<const void *>(kern), dim3(grid), dim3(threads), smem, st, pdl, args);
 }
 
 template <int TYPE>
-cudaError_t launch_type(bool tma, bool xres, const CUtensorMap &wm, const CUtensorMap &xm, const GemvArgs &a,
+cudaError_t launch_type(bool tma, bool xres, const GemvMaps &wm, const CUtensorMap &xm, const GemvArgs &a,
                         int grid, int threads, size_t smem, bool pdl, cudaStream_t st) {
-    if (tma) return xres ? launch_t<TYPE, true, true>(wm, xm, a, grid, threads, smem, pdl, st)
-                         : launch_t<TYPE, true, false>(wm, xm, a, grid, threads, smem, pdl, st);
-    return xres ? launch_t<TYPE, false, true>(wm, xm, a, grid, threads, smem, pdl, st)
-                : launch_t<TYPE, false, false>(wm, xm, a, grid, threads, smem, pdl, st);
+    if (a.nproj > 1) {
+        if (tma) return xres ? launch_t<TYPE, true, true, true>(wm, xm, a, grid, threads, smem, pdl, st)
+                             : launch_t<TYPE, true, false, true>(wm, xm, a, grid, threads, smem, pdl, st);
+        return xres ? launch_t<TYPE, false, true, true>(wm, xm, a, grid, threads, smem, pdl, st)
+                    : launch_t<TYPE, false, false, true>(wm, xm, a, grid, threads, smem, pdl, st);
+    }
+    if (tma) return xres ? launch_t<TYPE, true, true, false>(wm, xm, a, grid, threads, smem, pdl, st)
+                         : launch_t<TYPE, true, false, false>(wm, xm, a, grid, threads, smem, pdl, st);
+    return xres ? launch_t<TYPE, false, true, false>(wm, xm, a, grid, threads, smem, pdl, st)
+                : launch_t<TYPE, false, false, false>(wm, xm, a, grid, threads, smem, pdl, st);
 }
 
 }  // namespace
 
-cudaError_t gemv_launch(int type, const uint8_t *W, const __half *x, float *y, int64_t N, int64_t K, int M,
-                        unsigned *status, int num_sms, bool pdl, cudaStream_t stream) {
+cudaError_t gemv_launch_multi(int type, int nproj, const GemvProj *proj, const __half *x, int64_t K, int M,
+                              unsigned *status, int num_sms, bool pdl, cudaStream_t stream) {
     const int bb = block_bytes_of(type);
-    if (bb < 0 || M < 1 || M > kGemvMaxM) return cudaErrorInvalidValue;
-    GemvPlan pl = make_plan(type, N, K, M, num_sms);
+    if (bb < 0 || M < 1 || M > kGemvMaxM || nproj < 1 || nproj > kGemvMaxProj) return cudaErrorInvalidValue;
+    int tile0[kGemvMaxProj + 1];
+    int64_t T = 0;
+    for (int j = 0; j < nproj; ++j) {
+        tile0[j] = static_cast<int>(T);
+        T += (proj[j].N + 15) / 16;
+        if (T > (int64_t(1) << 30)) return cudaErrorInvalidValue;
+    }
+    tile0[nproj] = static_cast<int>(T);
+    GemvPlan pl = make_plan(type, T, K, M, num_sms);
     if (pl.smem > 227 * 1024) return cudaErrorNotSupported;
-    pl.a.W = W;
+    const int64_t row_bytes = K / 256 * bb;
+    for (int j = 0; j <= nproj; ++j) pl.a.tile0[j] = tile0[j];
+    for (int j = 0; j < nproj; ++j) {
+        pl.a.W[j] = proj[j].W;
+        pl.a.y[j] = proj[j].y;
+        pl.a.N[j] = static_cast<int>(proj[j].N);
+        pl.a.total_bytes[j] = proj[j].N * row_bytes;
+    }
+    pl.a.nproj = nproj;
     pl.a.x = x;
-    pl.a.y = y;
     pl.a.status = status;
-    CUtensorMap wm{}, xm{};
+    GemvMaps wm{};
+    CUtensorMap xm{};
     // x viewed as [M tokens][K/64 rows][64 halves]; one box = all tokens x (4 rows per
     // superblock of a warp slice or of a stage), 128-byte swizzled
     const uint32_t xbox_rows = static_cast<uint32_t>(4 * (pl.a.xres ? pl.a.kw : pl.a.S));
@@ -792,11 +836,13 @@ cudaError_t gemv_launch(int type, const uint8_t *W, const __half *x, float *y, i
                         static_cast<uint64_t>(M), 128, static_cast<uint64_t>(K) * 2, 64, xbox_rows,
                         static_cast<uint32_t>(M), true))
         return cudaErrorInvalidValue;
-    if (pl.tma) {   // W viewed as [N rows][row bytes / 8] of 8-byte elements
-        const uint64_t row_elems = static_cast<uint64_t>(K / 256) * bb / 8;
-        if (!encode_tmap_2d(&wm, CU_TENSOR_MAP_DATA_TYPE_UINT64, W, row_elems, static_cast<uint64_t>(N), row_elems * 8,
-                            static_cast<uint32_t>(pl.a.S * bb / 8), 16, false))
-            return cudaErrorInvalidValue;
+    if (pl.tma) {   // W[j] viewed as [N rows][row bytes / 8] of 8-byte elements
+        const uint64_t row_elems = static_cast<uint64_t>(row_bytes) / 8;
+        for (int j = 0; j < nproj; ++j)
+            if (!encode_tmap_2d(&wm.m[j], CU_TENSOR_MAP_DATA_TYPE_UINT64, proj[j].W, row_elems,
+                                static_cast<uint64_t>(proj[j].N), row_elems * 8, static_cast<uint32_t>(pl.a.S * bb / 8),
+                                16, false))
+                return cudaErrorInvalidValue;
     }
     const int threads = 32 * pl.warps;
     switch (type) {
@@ -806,6 +852,12 @@ cudaError_t gemv_launch(int type, const uint8_t *W, const __half *x, float *y, i
     case 23: return launch_type<23>(pl.tma, pl.a.xres != 0, wm, xm, pl.a, pl.grid, threads, pl.smem, pdl, stream);
     default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t gemv_launch(int type, const uint8_t *W, const __half *x, float *y, int64_t N, int64_t K, int M,
+                        unsigned *status, int num_sms, bool pdl, cudaStream_t stream) {
+    const GemvProj one{W, y, N};
+    return gemv_launch_multi(type, 1, &one, x, K, M, status, num_sms, pdl, stream);
 }
 
 }  // namespace ql

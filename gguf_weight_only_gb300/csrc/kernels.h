@@ -15,12 +15,26 @@ int block_bytes_of(int type);
 // ---------------------------------------------------------------- decode GEMV (gemv.cu)
 
 constexpr int kGemvMaxM = 8;
+constexpr int kGemvMaxProj = 4;
+
+// One projection of a multi-projection GEMV: W holds N rows of K/256 superblocks, y is [M, N].
+struct GemvProj {
+    const uint8_t *W;
+    float *y;
+    int64_t N;
+};
 
 // y[M <= 8, N] = x . dequant(W)^T, one launch. With `pdl` the kernel may start (and stream
 // its constant weights) while the preceding kernel in the stream finishes; it reads x and
 // writes y only after that kernel has completed.
 cudaError_t gemv_launch(int type, const uint8_t *W, const __half *x, float *y, int64_t N, int64_t K, int M,
                         unsigned *status, int num_sms, bool pdl, cudaStream_t stream);
+
+// y_j = x . dequant(W_j)^T for nproj <= kGemvMaxProj projections sharing x and K, in one launch:
+// the row tiles of all projections form one work list split over the persistent CTAs, and
+// each CTA's warps load their slice of x once for all of them.
+cudaError_t gemv_launch_multi(int type, int nproj, const GemvProj *proj, const __half *x, int64_t K, int M,
+                              unsigned *status, int num_sms, bool pdl, cudaStream_t stream);
 
 // ---------------------------------------------------------------- prefill GEMM (gemm_tc.cu)
 

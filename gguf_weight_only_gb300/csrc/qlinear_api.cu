@@ -117,6 +117,35 @@ int run(Path path, int type, const void *W, int64_t N, int64_t K, const void *x,
     return QL_OK;
 }
 
+// Several projections sharing x: each (W_j, N_j, y_j) is checked like a single call.
+int run_multi(int type, int n_proj, const void *const *W, const int64_t *N, int64_t K, const void *x, int64_t M,
+              float *const *y, void *stream) {
+    if (!W || !N || !y) return QL_ERR_NULL;
+    if (n_proj < 1 || n_proj > ql::kGemvMaxProj) return QL_ERR_SHAPE;
+    for (int j = 0; j < n_proj; ++j) {
+        const int rc = validate(type, W[j], N[j], K, x, M, y[j]);
+        if (rc != QL_OK) return rc;
+    }
+    DeviceState *s = nullptr;
+    int rc = device_state(&s);
+    if (rc != QL_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (M > ql::kGemvMaxM) {   // prefill: one GEMM per projection
+        for (int j = 0; j < n_proj; ++j) {
+            cudaError_t e = ql::gemm_launch(type, static_cast<const uint8_t *>(W[j]), static_cast<const __half *>(x),
+                                            y[j], N[j], K, M, s->status_word, s->num_sms, s->pdl, st);
+            if (e == cudaErrorNotSupported) return QL_ERR_UNSUPPORTED;
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+        return QL_OK;
+    }
+    ql::GemvProj proj[ql::kGemvMaxProj];
+    for (int j = 0; j < n_proj; ++j) proj[j] = ql::GemvProj{static_cast<const uint8_t *>(W[j]), y[j], N[j]};
+    cudaError_t e = ql::gemv_launch_multi(type, n_proj, proj, static_cast<const __half *>(x), K, static_cast<int>(M),
+                                          s->status_word, s->num_sms, s->pdl, st);
+    return e == cudaSuccess ? QL_OK : cuda_fail(e);
+}
+
 }  // namespace
 
 extern "C" {
@@ -135,6 +164,13 @@ int qlinear_gemm(int type, const void *W_blocks, int64_t N, int64_t K, const voi
                  void *stream) {
     return run(Path::Gemm, type, W_blocks, N, K, x_fp16, M, y_fp32, stream);
 }
+
+int qlinear_multi(int type, int n_proj, const void *const *W_blocks, const int64_t *N, int64_t K, const void *x_fp16,
+                  int64_t M, float *const *y_fp32, void *stream) {
+    return run_multi(type, n_proj, W_blocks, N, K, x_fp16, M, y_fp32, stream);
+}
+
+int qlinear_max_projections(void) { return ql::kGemvMaxProj; }
 
 int qlinear_block_bytes(int type) {
     const int b = ql::block_bytes_of(type);

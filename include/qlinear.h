@@ -89,6 +89,27 @@ int qlinear_gemv(int type, const void *W_blocks, int64_t N, int64_t K, const voi
 int qlinear_gemm(int type, const void *W_blocks, int64_t N, int64_t K, const void *x_fp16, int64_t M,
                  float *y_fp32, void *stream);
 
+/*
+ * qlinear_multi: several projections of the same activations in one pass,
+ *     y_j = x . dequant(W_j)^T          j < n_proj
+ * for weights that share `type` and K (a transformer's Q/K/V or gate/up projections). The
+ * pages fuse such pairs in their engine and check that the fused result equals the separate
+ * layers (test/unit/test_llm_quant_cpu.py, test_q8_linear_pair_matches_separate).
+ * For M <= qlinear_gemv_max_m() one decode launch covers all projections: the row tiles of
+ * every W_j form one work list split evenly over the SMs, and each slice of x is loaded once;
+ * for larger M each projection runs the prefill kernel in turn.
+ * Arguments: n_proj in [1, qlinear_max_projections()]; W_blocks, N and y_fp32 are HOST arrays
+ * of n_proj entries (W_blocks[j] and y_fp32[j] are device pointers with the layouts and
+ * alignment of qlinear(), y_fp32[j] holding M*N[j] floats); K, x_fp16, M, stream as in
+ * qlinear(). Every projection is validated as a qlinear() call; NULL arrays give QL_ERR_NULL
+ * and n_proj out of range QL_ERR_SHAPE, with nothing enqueued. The outputs must not overlap.
+ */
+int qlinear_multi(int type, int n_proj, const void *const *W_blocks, const int64_t *N, int64_t K,
+                  const void *x_fp16, int64_t M, float *const *y_fp32, void *stream);
+
+/* Most projections one qlinear_multi() call takes (4). */
+int qlinear_max_projections(void);
+
 /* Bytes per 256-weight superblock of `type` (144/176/210/136), or QL_ERR_TYPE. */
 int qlinear_block_bytes(int type);
 

@@ -85,3 +85,43 @@ def test_python_wrapper_raises_without_cuda_tensors(lib):
     import torch
     with pytest.raises(TypeError):
         ql.qlinear(torch.zeros(144, dtype=torch.uint8), 12, 1, 256, torch.zeros(1, 256, dtype=torch.float16))
+
+
+# ------------------------------------------------------------------ qlinear_multi (projections sharing x)
+
+def _multi(lib, t, W, N, K, x, M, y, n):
+    k = max(len(W or N or y), 1)
+    Wa = (ctypes.c_void_p * k)(*[w or None for w in W]) if W is not None else None
+    Na = (ctypes.c_int64 * k)(*N) if N is not None else None
+    Ya = (ctypes.c_void_p * k)(*[v or None for v in y]) if y is not None else None
+    return lib.qlinear_multi(t, n, Wa, Na, K, ctypes.c_void_p(x or None), M, Ya, None)
+
+
+def test_max_projections(lib):
+    assert ql.max_projections() == 4
+
+
+MULTI_BAD = [
+    # (type, [W], [N], K, x, M, [y], n_proj override, expected)
+    (12, None, [8, 8], 256, 16, 1, [16, 32], 2, -3),              # NULL W array
+    (12, [16, 32], None, 256, 16, 1, [16, 32], 2, -3),            # NULL N array
+    (12, [16, 32], [8, 8], 256, 16, 1, None, 2, -3),              # NULL y array
+    (12, [16], [8], 256, 16, 1, [16], 0, -2),                     # no projection
+    (12, [16] * 5, [8] * 5, 256, 16, 1, [16] * 5, 5, -2),         # more than 4
+    (7, [16, 32], [8, 8], 256, 16, 1, [16, 32], 2, -1),           # unsupported type
+    (12, [16, 32], [8, 8], 300, 16, 1, [16, 32], 2, -2),          # K not a multiple of 256
+    (12, [16, 32], [8, 0], 256, 16, 1, [16, 32], 2, -2),          # second projection N < 1
+    (12, [16, 32], [8, 8], 256, 16, 0, [16, 32], 2, -2),          # M < 1
+    (12, [16, 0], [8, 8], 256, 16, 1, [16, 32], 2, -3),           # second W NULL
+    (12, [16, 32], [8, 8], 256, 0, 1, [16, 32], 2, -3),           # x NULL
+    (12, [16, 32], [8, 8], 256, 16, 1, [16, 0], 2, -3),           # second y NULL
+    (12, [16, 40], [8, 8], 256, 16, 1, [16, 32], 2, -4),          # second W misaligned
+    (12, [16, 32], [8, 8], 256, 24, 1, [16, 32], 2, -4),          # x misaligned
+    (12, [16, 32, 48], [8, 8, 8], 256, 16, 1, [16, 32, 52], 3, -4),  # third y misaligned
+]
+
+
+@pytest.mark.parametrize("case", MULTI_BAD)
+def test_multi_bad_arguments_rejected_before_launch(lib, case):
+    t, W, N, K, x, M, y, n, expect = case
+    assert _multi(lib, t, W, N, K, x, M, y, n) == expect

@@ -386,6 +386,59 @@ def time_multi(t, K, Ns, M, reps, dev, stream, l2, lib, fused=True, replays=5):
     return float(np.median(times))
 
 
+def time_fused(kind, t, K, N, M, reps, dev, stream, l2, lib, replays=5):
+    """As time_shape, for a decode call with a fused prologue ("silu": x = silu(gate) * up;
+    "rmsnorm": x = rmsnorm(h) * w) and a residual added in place. Returns ms per call."""
+    import torch
+    wb = N * (K // 256) * BB[t]
+    Pk = max(2, int(np.ceil(2.2 * l2 / wb)))
+    W0 = torch.from_numpy(synth.weights(t, N, K, [7, t, K, N])).to(dev)
+    Wk = [W0.clone() for _ in range(Pk)]
+    rng = np.random.default_rng([9, t, K, N, M])
+    a = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float16 if kind == "silu" else np.float32)).to(dev)
+    b = torch.from_numpy(rng.standard_normal((M, K) if kind == "silu" else (K,)).astype(np.float32)).to(dev)
+    y = torch.zeros((M, N), dtype=torch.float32, device=dev)
+    sh = stream.cuda_stream
+
+    def call(i):
+        if kind == "silu":
+            rc = lib.qlinear_silu_mul(t, Wk[i % Pk].data_ptr(), N, K, a.data_ptr(), b.data_ptr(), M, y.data_ptr(),
+                                      y.data_ptr(), sh)
+        else:
+            rc = lib.qlinear_rmsnorm(t, Wk[i % Pk].data_ptr(), N, K, a.data_ptr(), b.data_ptr(), 1e-6, M, y.data_ptr(),
+                                     y.data_ptr(), None, sh)
+        if rc != 0:
+            raise RuntimeError(f"fused {kind} failed: {rc}")
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            call(i)
+    torch.cuda.synchronize(dev)
+    gk = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gk, stream=stream):
+        for i in range(reps):
+            call(i)
+    with torch.cuda.stream(stream):
+        gk.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for _ in range(replays):
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            gk.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(e0.elapsed_time(e1) / reps)
+    del gk, Wk
+    torch.cuda.empty_cache()
+    return float(np.median(times))
+
+
+# Fused decode calls: kind, type, K, N, M (the 8B down projection fed by the SiLU gate, the
+# 8B gate projection fed by RMSNorm)
+TABLE_FUSED = [("silu", 12, 12288, 4096, 1), ("rmsnorm", 12, 4096, 12288, 1)]
+
 # Projection sets sharing x (one qlinear_multi call each): name, type, K, (N_j), M
 TABLE_MULTI = [
     ("8B Q/K/V", 12, 4096, (4096, 1024, 1024), 1),
@@ -440,6 +493,15 @@ def run_table(args):
                                                      "frac": round(byts / (ms * 1e-3) / 1e9 / hbm, 4)}
         print(json.dumps({"projections": name, "type": TYPE_NAMES[t], "K": K, "N": list(Ns), "M": M, **res,
                           "peak_kind": peak_kind, "status": ql.device_status()}), flush=True)
+    for kind, t, K, N, M in TABLE_FUSED:
+        ms = time_fused(kind, t, K, N, M, 200, dev, stream, l2, lib)
+        plain = time_shape(t, K, N, M, lib.qlinear, 200, dev, stream, l2, replays=5)
+        # weights + the prologue's inputs (gate fp16 and up fp32, or h and w fp32) + residual and y
+        byts = N * (K // 256) * BB[t] + (6 * M * K if kind == "silu" else 4 * M * K + 4 * K) + 8 * M * N
+        print(json.dumps({"fused": kind, "type": TYPE_NAMES[t], "K": K, "N": N, "M": M, "us": round(ms * 1e3, 2),
+                          "GBs": round(byts / (ms * 1e-3) / 1e9, 1), "frac": round(byts / (ms * 1e-3) / 1e9 / hbm, 4),
+                          "plain_us": round(plain * 1e3, 2), "peak_kind": peak_kind,
+                          "status": ql.device_status()}), flush=True)
 
 
 # ---------------------------------------------------------------------------- oracle on the CPU

@@ -23,7 +23,8 @@ STATUS = {0: "QL_OK", -1: "QL_ERR_TYPE", -2: "QL_ERR_SHAPE", -3: "QL_ERR_NULL", 
 # against the header).
 EXPORTS = ("qlinear", "qlinear_gemv", "qlinear_gemm", "qlinear_block_bytes", "qlinear_gemv_max_m",
            "qlinear_strerror", "qlinear_last_cuda_error", "qlinear_device_status", "qlinear_launch_count",
-           "qlinear_selftest_wait_timeout", "qlinear_multi", "qlinear_max_projections")
+           "qlinear_selftest_wait_timeout", "qlinear_multi", "qlinear_max_projections", "qlinear_silu_mul",
+           "qlinear_rmsnorm")
 
 _lib = None
 
@@ -65,6 +66,10 @@ def lib() -> ctypes.CDLL:
         l.qlinear_multi.restype = ctypes.c_int
         l.qlinear_max_projections.argtypes = []
         l.qlinear_max_projections.restype = ctypes.c_int
+        l.qlinear_silu_mul.argtypes = [ctypes.c_int, vp, i64, i64, vp, vp, i64, vp, vp, vp]
+        l.qlinear_silu_mul.restype = ctypes.c_int
+        l.qlinear_rmsnorm.argtypes = [ctypes.c_int, vp, i64, i64, vp, vp, ctypes.c_float, i64, vp, vp, vp, vp]
+        l.qlinear_rmsnorm.restype = ctypes.c_int
         _lib = l
     return _lib
 
@@ -179,6 +184,67 @@ def qlinear_multi(Ws, ggml_type: int, Ns, K: int, x, outs=None, stream=None):
     _check(lib().qlinear_multi(int(ggml_type), n, w_arr, n_arr, int(K), x.data_ptr(), M, y_arr,
                                _stream_handle(stream)), "qlinear_multi")
     return outs
+
+
+def _mk(x, dtype, shape, what):
+    import torch
+    if not (isinstance(x, torch.Tensor) and x.is_cuda and x.dtype == dtype and x.is_contiguous()):
+        raise TypeError(f"{what} must be a contiguous {dtype} CUDA tensor")
+    n = 1
+    for d in shape:
+        n *= int(d)
+    if x.numel() != n:
+        raise ValueError(f"{what} must have {n} elements (shape {tuple(shape)})")
+    return x
+
+
+def _fused_common(W, ggml_type, N, K, M, residual, out, dev):
+    import torch
+    if not (isinstance(W, torch.Tensor) and W.is_cuda and W.dtype == torch.uint8 and W.is_contiguous()):
+        raise TypeError("W must be a contiguous uint8 CUDA tensor")
+    bb = block_bytes(ggml_type)
+    if bb > 0 and W.numel() < N * (K // 256) * bb:
+        raise ValueError("W holds fewer bytes than N*K/256 superblocks")
+    if residual is not None:
+        _mk(residual, torch.float32, (M, N), "residual")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=dev)
+    else:
+        _mk(out, torch.float32, (M, N), "out")
+    return out
+
+
+def qlinear_silu_mul(W, ggml_type: int, N: int, K: int, gate, up, residual=None, out=None, stream=None):
+    """y = fp16(silu(gate) * up) . dequant(W)^T (+ residual), one decode launch (M <= 8).
+    gate: float16 (M, K); up: float32 (M, K); residual: float32 (M, N) or None (may be out)."""
+    import torch
+    M = gate.shape[0] if gate.dim() == 2 else 1
+    _mk(gate, torch.float16, (M, K), "gate")
+    _mk(up, torch.float32, (M, K), "up")
+    out = _fused_common(W, ggml_type, N, K, M, residual, out, gate.device)
+    _check(lib().qlinear_silu_mul(int(ggml_type), W.data_ptr(), int(N), int(K), gate.data_ptr(), up.data_ptr(), M,
+                                  residual.data_ptr() if residual is not None else None, out.data_ptr(),
+                                  _stream_handle(stream)), "qlinear_silu_mul")
+    return out
+
+
+def qlinear_rmsnorm(W, ggml_type: int, N: int, K: int, h, norm_w, eps: float, residual=None, out=None, xnorm=None,
+                    stream=None):
+    """y = fp16(h * rsqrt(mean(h^2) + eps) * norm_w) . dequant(W)^T (+ residual), one decode
+    launch (M <= 8). h: float32 (M, K); norm_w: float32 (K,); xnorm: optional float16 (M, K)
+    that receives the normalised fp16 activations."""
+    import torch
+    M = h.shape[0] if h.dim() == 2 else 1
+    _mk(h, torch.float32, (M, K), "h")
+    _mk(norm_w, torch.float32, (K,), "norm_w")
+    if xnorm is not None:
+        _mk(xnorm, torch.float16, (M, K), "xnorm")
+    out = _fused_common(W, ggml_type, N, K, M, residual, out, h.device)
+    _check(lib().qlinear_rmsnorm(int(ggml_type), W.data_ptr(), int(N), int(K), h.data_ptr(), norm_w.data_ptr(),
+                                 float(eps), M, residual.data_ptr() if residual is not None else None, out.data_ptr(),
+                                 xnorm.data_ptr() if xnorm is not None else None, _stream_handle(stream)),
+           "qlinear_rmsnorm")
+    return out
 
 
 def device_status(stream=None) -> int:

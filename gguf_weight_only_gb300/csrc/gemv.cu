@@ -80,6 +80,15 @@ struct GemvArgs {
     int nproj;
     const __half *x;
     unsigned *status;
+    // Fused prologue (resident x only): 0 = x given; 1 = x = fp16(silu(gate) * up);
+    // 2 = x = fp16(h * rsqrt(mean(h^2) + eps) * norm_w), also written to xnorm when set.
+    int pro;
+    const __half *gate;      // pro 1: [M, K]
+    const float *up_or_h;    // pro 1: up [M, K]; pro 2: h [M, K]
+    const float *norm_w;     // pro 2: [K]
+    float eps;
+    __half *xnorm;           // pro 2: optional [M, K] output of the normalised activations
+    const float *residual;   // optional [M, N] added to y (single projection); may be y itself
     int K, M, nsb;
     int S;                   // superblocks per stage
     int kw;                  // superblocks of the K slice each warp owns
@@ -406,6 +415,69 @@ __device__ __forceinline__ void superblock_iq4(uint32_t blk_a, uint32_t blk_b, c
     acc[3] += db * (d1[3] + e1[3]);
 }
 
+// ---------------------------------------------------------------- fused prologues
+
+// Shared-memory scratch of the RMSNorm prologue, in the free tail of the first (barrier)
+// kilobyte: per-warp partial sums of h^2 for each token.
+constexpr uint32_t kSqOffset = 512;
+
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// silu(g) * u in fp32: g / (1 + e^-g), with e^-g capped at e^80 (where silu rounds to 0 in
+// fp16 anyway) so that the fast division stays in its exact range. __expf and __fdividef err
+// by a few fp32 ulp, far below the fp16 rounding that follows.
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    return __fdividef(g, 1.0f + __expf(fminf(-g, 80.0f))) * u;
+}
+
+// Inputs of eight consecutive activations x[tok][k0 .. k0+7] of a fused prologue.
+struct ChunkIn {
+    uint4 gate;          // pro 1: 8 fp16
+    float4 a0, a1;       // pro 1: up; pro 2: h
+    float4 w0, w1;       // pro 2: norm weight
+};
+
+__device__ __forceinline__ ChunkIn chunk_load(const GemvArgs &p, int tok, int64_t k0) {
+    ChunkIn c;
+    const int64_t o = static_cast<int64_t>(tok) * p.K + k0;
+    c.a0 = __ldg(reinterpret_cast<const float4 *>(p.up_or_h + o));
+    c.a1 = __ldg(reinterpret_cast<const float4 *>(p.up_or_h + o) + 1);
+    if (p.pro == 1) {
+        c.gate = __ldg(reinterpret_cast<const uint4 *>(p.gate + o));
+    } else {
+        c.w0 = __ldg(reinterpret_cast<const float4 *>(p.norm_w + k0));
+        c.w1 = __ldg(reinterpret_cast<const float4 *>(p.norm_w + k0) + 1);
+    }
+    return c;
+}
+
+// The eight activations as fp16 in k order, each rounded once from fp32.
+__device__ __forceinline__ uint4 chunk_compute(const GemvArgs &p, const ChunkIn &c, float rstd) {
+    float v[8];
+    if (p.pro == 1) {
+        const __half2 *g2 = reinterpret_cast<const __half2 *>(&c.gate);
+        const float2 g0 = __half22float2(g2[0]), g1 = __half22float2(g2[1]);
+        const float2 g2f = __half22float2(g2[2]), g3 = __half22float2(g2[3]);
+        v[0] = silu_mul(g0.x, c.a0.x); v[1] = silu_mul(g0.y, c.a0.y);
+        v[2] = silu_mul(g1.x, c.a0.z); v[3] = silu_mul(g1.y, c.a0.w);
+        v[4] = silu_mul(g2f.x, c.a1.x); v[5] = silu_mul(g2f.y, c.a1.y);
+        v[6] = silu_mul(g3.x, c.a1.z); v[7] = silu_mul(g3.y, c.a1.w);
+    } else {
+        v[0] = c.a0.x * rstd * c.w0.x; v[1] = c.a0.y * rstd * c.w0.y;
+        v[2] = c.a0.z * rstd * c.w0.z; v[3] = c.a0.w * rstd * c.w0.w;
+        v[4] = c.a1.x * rstd * c.w1.x; v[5] = c.a1.y * rstd * c.w1.y;
+        v[6] = c.a1.z * rstd * c.w1.z; v[7] = c.a1.w * rstd * c.w1.w;
+    }
+    return make_uint4(pack_half2(v[0], v[1]), pack_half2(v[2], v[3]), pack_half2(v[4], v[5]), pack_half2(v[6], v[7]));
+}
+
+// Chunks a lane fills per group of a fused prologue: their global loads are all issued before
+// any is used.
+constexpr int kFillGroup = 4;
+
 // ---------------------------------------------------------------- the kernel
 //
 // Persistent: CTA b owns a contiguous run of 16-row tiles (an equal share of the T tiles of all
@@ -416,7 +488,7 @@ __device__ __forceinline__ void superblock_iq4(uint32_t blk_a, uint32_t blk_b, c
 // next unit as soon as it has consumed it, across tile boundaries. The warps' 16 x 8 partial
 // tiles go to shared memory; after each round of tiles they are summed in fixed order.
 
-template <int TYPE, bool TMA, bool XRES, bool MULTI>
+template <int TYPE, bool TMA, bool XRES, bool MULTI, bool PRO>
 __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const __grid_constant__ GemvMaps wmaps,
                                                       const __grid_constant__ CUtensorMap xmap,
                                                       const __grid_constant__ GemvArgs p) {
@@ -446,9 +518,12 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
     auto tile_rows = [&](int t, int &j) {
         const int gt = t_begin + t;
         j = 0;
-        if constexpr (!MULTI) return 16 * gt;   // one projection: the lookup cost 3-4% on GB300
-        while (j + 1 < p.nproj && gt >= p.tile0[j + 1]) ++j;
-        return 16 * (gt - p.tile0[j]);
+        if constexpr (!MULTI) {
+            return 16 * gt;   // one projection: the lookup cost 3-4% on GB300
+        } else {
+            while (j + 1 < p.nproj && gt >= p.tile0[j + 1]) ++j;
+            return 16 * (gt - p.tile0[j]);
+        }
     };
 
     // warp = (tile group tg, K slice kidx): it owns superblocks [kb0, kb1) of the CTA's tiles
@@ -464,7 +539,7 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
     if (lane == 0) {
         for (int s = 0; s <= D; ++s) mbar_init(bar0 + 8 * s, 1);
         fence_mbar_init();
-        prefetch_tmap(&xmap);
+        if constexpr (!PRO) prefetch_tmap(&xmap);
         if constexpr (TMA)
             for (int j = 0; j < p.nproj; ++j) prefetch_tmap(&wmaps.m[j]);
     }
@@ -538,22 +613,49 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
     if constexpr (XRES) {
         for (int s = 0; s < D && s < total; ++s) issue_next(s);
         pdl_wait();
-        if (nmine > 0 && lane == 0) {   // this warp's x slice, all tokens, once
-            mbar_arrive_expect_tx(xbar, p.x_tx);
-            tma_load_3d(xreg, &xmap, 0, kb0 * 4, 0, xbar);
+        float *const sq = reinterpret_cast<float *>(gbase + kSqOffset);   // [warp][token]
+        if (PRO && p.pro == 2) {
+            // sum of h^2 per token: each warp a strided share of the row, fixed order
+            const int kstep = static_cast<int>(blockDim.x) * 4;
+            for (int m = 0; m < p.M; ++m) {
+                const float *hrow = p.up_or_h + static_cast<int64_t>(m) * p.K;
+                float acc2 = 0.f;
+                for (int k0 = (warp * 32 + lane) * 4; k0 < p.K; k0 += 8 * kstep) {
+                    float4 h[8];   // eight independent loads in flight, then summed in order
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        h[i] = k0 + i * kstep < p.K ? __ldg(reinterpret_cast<const float4 *>(hrow + k0 + i * kstep))
+                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc2 += (h[i].x * h[i].x + h[i].y * h[i].y) + (h[i].z * h[i].z + h[i].w * h[i].w);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) acc2 += __shfl_xor_sync(0xFFFFFFFFu, acc2, o);
+                if (lane == 0) sq[warp * kGemvMaxM + m] = acc2;
+            }
+            __syncthreads();   // every warp of the CTA runs this set-up
         }
-        if (nmine > 0) ok = mbar_wait(xbar, 0);
-        if constexpr (PERM) {
-            // One pass over the warp's x tile: [x0 x1 x2 x3] -> [x0 x2 x1 x3] inside every 16-byte
-            // chunk and, for the K-quants, the sums of x over each 32-wide sub-block. The tile is
+        if constexpr (!PRO) {
+            if (nmine > 0 && lane == 0) {   // this warp's x slice, all tokens, once
+                mbar_arrive_expect_tx(xbar, p.x_tx);
+                tma_load_3d(xreg, &xmap, 0, kb0 * 4, 0, xbar);
+            }
+            if (nmine > 0) ok = mbar_wait(xbar, 0);
+        }
+        if constexpr (PERM || PRO) {
+            // One pass over the warp's x tile: fill it (fused prologue), permute it in place
+            // [x0 x1 x2 x3] -> [x0 x2 x1 x3] inside every 16-byte chunk (K-quants, Q6_K) and,
+            // for the K-quants, store the sums of x over each 32-wide sub-block. The tile is
             // 128-byte rows r = token * 4 kw + 4 * superblock + segment with chunk c of a row
             // stored at c ^ (r & 7); that swizzle keeps each aligned group of four chunks (one
             // sub-block) together, so four neighbouring lanes hold one sub-block and two shuffles
             // sum it. x_tx / 16 is a multiple of 32: every lane runs every pass.
-            for (uint32_t q = lane; q < p.x_tx / 16u; q += 32) {
-                const uint4 v = lds128(xreg + 16u * q);
-                sts128(xreg + 16u * q, make_uint4(prmt(v.x, v.y, 0x5410u), prmt(v.x, v.y, 0x7632u),
-                                                  prmt(v.z, v.w, 0x5410u), prmt(v.z, v.w, 0x7632u)));
+            auto put = [&](uint32_t q, const uint4 &v) {   // store chunk q (k order) permuted, add its sums
+                if constexpr (PERM)
+                    sts128(xreg + 16u * q, make_uint4(prmt(v.x, v.y, 0x5410u), prmt(v.x, v.y, 0x7632u),
+                                                      prmt(v.z, v.w, 0x5410u), prmt(v.z, v.w, 0x7632u)));
+                else
+                    sts128(xreg + 16u * q, v);
                 if constexpr (XSUM) {
                     const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
                     const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
@@ -569,6 +671,49 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
                         __half *rec = reinterpret_cast<__half *>(gbase + (xsum_base - base) + (r >> 2) * 32u + 8u * (r & 3u));
                         rec[half] = hi;
                         rec[2 + half] = lo;
+                    }
+                }
+            };
+            const uint32_t nq = p.x_tx / 16u;
+            if constexpr (!PRO) {
+                for (uint32_t q = lane; q < nq; q += 32) put(q, lds128(xreg + 16u * q));
+            } else {
+                // chunk q holds columns k0 .. k0+7 of token tokq (the tile's swizzle undone)
+                const uint32_t xrows_tok = 4u * static_cast<uint32_t>(p.kw);
+                auto chunk_pos = [&](uint32_t q, uint32_t &tokq) {
+                    const uint32_t r = q >> 3;
+                    tokq = r / xrows_tok;
+                    const uint32_t seg = r - tokq * xrows_tok;
+                    return (static_cast<int64_t>(kb0) * 4 + seg) * 64 + 8 * ((q & 7u) ^ (r & 7u));
+                };
+                for (uint32_t q0 = lane; q0 < nq; q0 += 32u * kFillGroup) {   // nq is a multiple of 32: uniform
+                    ChunkIn in[kFillGroup];
+#pragma unroll
+                    for (int i = 0; i < kFillGroup; ++i) {
+                        uint32_t tokq;
+                        const uint32_t q = q0 + 32u * i;
+                        const int64_t k0 = chunk_pos(q, tokq);
+                        if (q < nq && k0 < p.K) in[i] = chunk_load(p, static_cast<int>(tokq), k0);
+                    }
+#pragma unroll
+                    for (int i = 0; i < kFillGroup; ++i) {
+                        uint32_t tokq;
+                        const uint32_t q = q0 + 32u * i;
+                        if (q >= nq) break;
+                        const int64_t k0 = chunk_pos(q, tokq);
+                        uint4 v = make_uint4(0u, 0u, 0u, 0u);   // columns beyond K (a partial last slice)
+                        if (k0 < p.K) {
+                            float rstd = 0.f;
+                            if (p.pro == 2) {
+                                float tot = 0.f;
+                                for (int w2 = 0; w2 < static_cast<int>(blockDim.x >> 5); ++w2) tot += sq[w2 * kGemvMaxM + tokq];
+                                rstd = rsqrtf(tot / static_cast<float>(p.K) + p.eps);
+                            }
+                            v = chunk_compute(p, in[i], rstd);
+                            if (p.pro == 2 && p.xnorm && b == 0 && tg == 0)   // one writer per element
+                                *reinterpret_cast<uint4 *>(p.xnorm + static_cast<int64_t>(tokq) * p.K + k0) = v;
+                        }
+                        put(q, v);
                     }
                 }
             }
@@ -649,7 +794,11 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
           for (int kk = 0; kk < p.ks; ++kk) sum += src[kk * per_tile];
           int jp;
           const int row = tile_rows(round0 + tt, jp) + (rem & 15);
-          if (row < p.N[jp]) p.y[jp][static_cast<int64_t>(rem >> 4) * p.N[jp] + row] = sum;
+          if (row < p.N[jp]) {
+              const int64_t o = static_cast<int64_t>(rem >> 4) * p.N[jp] + row;
+              if constexpr (PRO) p.y[jp][o] = p.residual ? sum + p.residual[o] : sum;   // y may be the residual
+              else p.y[jp][o] = sum;
+          }
       }
       if (rend < ntiles) __syncthreads();   // the next round reuses the slots
     }
@@ -669,8 +818,9 @@ struct GemvPlan {
     size_t smem;
 };
 
-// T: 16-row tiles over all projections.
-GemvPlan make_plan(int type, int64_t T, int64_t K, int M, int num_sms) {
+// T: 16-row tiles over all projections. need_xres: only plans with x resident per warp (the
+// fused prologues fill that tile).
+GemvPlan make_plan(int type, int64_t T, int64_t K, int M, int num_sms, bool need_xres) {
     GemvPlan pl{};
     GemvArgs &a = pl.a;
     const int bb = block_bytes_of(type);
@@ -740,7 +890,7 @@ GemvPlan make_plan(int type, int64_t T, int64_t K, int M, int num_sms) {
         w = ks * tgc;
         // partials of up to round_tiles tiles (16 KB of shared memory) are reduced per round
         round_tiles = std::max(1, std::min(tmax, (16 * 1024) / (ks * 16 * M * 4)));
-        for (int xres = 1; xres >= 0 && !found; --xres) {
+        for (int xres = 1; xres >= (need_xres ? 1 : 0) && !found; --xres) {
             for (int S = std::min(kw, s_max); S >= s_mult && !found; S -= s_mult) {
                 const int nst = (kw + S - 1) / S;
                 for (int D = std::min(4, std::max(2, 2 * nst)); D >= 2 && !found; --D) {
@@ -750,7 +900,7 @@ GemvPlan make_plan(int type, int64_t T, int64_t K, int M, int num_sms) {
             }
         }
     }
-    if (!found) {
+    if (!found || w * (a.stages + 1) * 8 > static_cast<int>(kSqOffset)) {   // barriers end before the prologue scratch
         pl.smem = SIZE_MAX;
         return pl;
     }
@@ -769,10 +919,10 @@ GemvPlan make_plan(int type, int64_t T, int64_t K, int M, int num_sms) {
     return pl;
 }
 
-template <int TYPE, bool TMA, bool XRES, bool MULTI>
+template <int TYPE, bool TMA, bool XRES, bool MULTI, bool PRO = false>
 cudaError_t launch_t(const GemvMaps &wm, const CUtensorMap &xm, const GemvArgs &a, int grid, int threads,
                      size_t smem, bool pdl, cudaStream_t st) {
-    auto kern = gemv_kernel<TYPE, TMA, XRES, MULTI>;
+    auto kern = gemv_kernel<TYPE, TMA, XRES, MULTI, PRO>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -788,6 +938,11 @@ cudaError_t launch_t(const GemvMaps &wm, const CUtensorMap &xm, const GemvArgs &
 template <int TYPE>
 cudaError_t launch_type(bool tma, bool xres, const GemvMaps &wm, const CUtensorMap &xm, const GemvArgs &a,
                         int grid, int threads, size_t smem, bool pdl, cudaStream_t st) {
+    if (a.pro != 0) {   // fused prologues: one projection, x resident (the plan guarantees it)
+        if (a.nproj != 1 || !xres) return cudaErrorInvalidValue;
+        return tma ? launch_t<TYPE, true, true, false, true>(wm, xm, a, grid, threads, smem, pdl, st)
+                   : launch_t<TYPE, false, true, false, true>(wm, xm, a, grid, threads, smem, pdl, st);
+    }
     if (a.nproj > 1) {
         if (tma) return xres ? launch_t<TYPE, true, true, true>(wm, xm, a, grid, threads, smem, pdl, st)
                              : launch_t<TYPE, true, false, true>(wm, xm, a, grid, threads, smem, pdl, st);
@@ -802,10 +957,14 @@ cudaError_t launch_type(bool tma, bool xres, const GemvMaps &wm, const CUtensorM
 
 }  // namespace
 
-cudaError_t gemv_launch_multi(int type, int nproj, const GemvProj *proj, const __half *x, int64_t K, int M,
-                              unsigned *status, int num_sms, bool pdl, cudaStream_t stream) {
+namespace {
+
+cudaError_t launch_impl(int type, int nproj, const GemvProj *proj, const __half *x, int64_t K, int M,
+                        const GemvFusion *fu, unsigned *status, int num_sms, bool pdl, cudaStream_t stream) {
     const int bb = block_bytes_of(type);
     if (bb < 0 || M < 1 || M > kGemvMaxM || nproj < 1 || nproj > kGemvMaxProj) return cudaErrorInvalidValue;
+    const int pro = fu ? fu->pro : 0;
+    if (pro < 0 || pro > 2 || (fu && fu->residual && nproj != 1)) return cudaErrorInvalidValue;
     int tile0[kGemvMaxProj + 1];
     int64_t T = 0;
     for (int j = 0; j < nproj; ++j) {
@@ -814,7 +973,7 @@ cudaError_t gemv_launch_multi(int type, int nproj, const GemvProj *proj, const _
         if (T > (int64_t(1) << 30)) return cudaErrorInvalidValue;
     }
     tile0[nproj] = static_cast<int>(T);
-    GemvPlan pl = make_plan(type, T, K, M, num_sms);
+    GemvPlan pl = make_plan(type, T, K, M, num_sms, pro != 0);
     if (pl.smem > 227 * 1024) return cudaErrorNotSupported;
     const int64_t row_bytes = K / 256 * bb;
     for (int j = 0; j <= nproj; ++j) pl.a.tile0[j] = tile0[j];
@@ -827,14 +986,23 @@ cudaError_t gemv_launch_multi(int type, int nproj, const GemvProj *proj, const _
     pl.a.nproj = nproj;
     pl.a.x = x;
     pl.a.status = status;
+    if (fu) {
+        pl.a.pro = pro;
+        pl.a.gate = fu->gate;
+        pl.a.up_or_h = fu->up_or_h;
+        pl.a.norm_w = fu->norm_w;
+        pl.a.eps = fu->eps;
+        pl.a.xnorm = fu->xnorm;
+        pl.a.residual = fu->residual;
+    }
     GemvMaps wm{};
     CUtensorMap xm{};
     // x viewed as [M tokens][K/64 rows][64 halves]; one box = all tokens x (4 rows per
     // superblock of a warp slice or of a stage), 128-byte swizzled
     const uint32_t xbox_rows = static_cast<uint32_t>(4 * (pl.a.xres ? pl.a.kw : pl.a.S));
-    if (!encode_tmap_3d(&xm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, 64, static_cast<uint64_t>(K / 64),
-                        static_cast<uint64_t>(M), 128, static_cast<uint64_t>(K) * 2, 64, xbox_rows,
-                        static_cast<uint32_t>(M), true))
+    if (pro == 0 && !encode_tmap_3d(&xm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, 64, static_cast<uint64_t>(K / 64),
+                                    static_cast<uint64_t>(M), 128, static_cast<uint64_t>(K) * 2, 64, xbox_rows,
+                                    static_cast<uint32_t>(M), true))
         return cudaErrorInvalidValue;
     if (pl.tma) {   // W[j] viewed as [N rows][row bytes / 8] of 8-byte elements
         const uint64_t row_elems = static_cast<uint64_t>(row_bytes) / 8;
@@ -854,10 +1022,23 @@ cudaError_t gemv_launch_multi(int type, int nproj, const GemvProj *proj, const _
     }
 }
 
+}  // namespace
+
+cudaError_t gemv_launch_multi(int type, int nproj, const GemvProj *proj, const __half *x, int64_t K, int M,
+                              unsigned *status, int num_sms, bool pdl, cudaStream_t stream) {
+    return launch_impl(type, nproj, proj, x, K, M, nullptr, status, num_sms, pdl, stream);
+}
+
 cudaError_t gemv_launch(int type, const uint8_t *W, const __half *x, float *y, int64_t N, int64_t K, int M,
                         unsigned *status, int num_sms, bool pdl, cudaStream_t stream) {
     const GemvProj one{W, y, N};
-    return gemv_launch_multi(type, 1, &one, x, K, M, status, num_sms, pdl, stream);
+    return launch_impl(type, 1, &one, x, K, M, nullptr, status, num_sms, pdl, stream);
+}
+
+cudaError_t gemv_launch_fused(int type, const uint8_t *W, float *y, int64_t N, int64_t K, int M, const GemvFusion &f,
+                              unsigned *status, int num_sms, bool pdl, cudaStream_t stream) {
+    const GemvProj one{W, y, N};
+    return launch_impl(type, 1, &one, nullptr, K, M, &f, status, num_sms, pdl, stream);
 }
 
 }  // namespace ql

@@ -36,6 +36,19 @@ cudaError_t gemv_launch(int type, const uint8_t *W, const __half *x, float *y, i
 cudaError_t gemv_launch_multi(int type, int nproj, const GemvProj *proj, const __half *x, int64_t K, int M,
                               unsigned *status, int num_sms, bool pdl, cudaStream_t stream);
 
+// Fused producer of x and consumer of y for one decode launch (M <= kGemvMaxM).
+struct GemvFusion {
+    int pro = 0;                     // 1: x = fp16(silu(gate) * up); 2: x = fp16(rmsnorm(h) * norm_w)
+    const __half *gate = nullptr;    // pro 1: [M, K] fp16
+    const float *up_or_h = nullptr;  // pro 1: up [M, K]; pro 2: h [M, K]
+    const float *norm_w = nullptr;   // pro 2: [K]
+    float eps = 0.f;                 // pro 2
+    __half *xnorm = nullptr;         // pro 2: optional [M, K] copy of the fp16 normalised x
+    const float *residual = nullptr; // optional [M, N], added to y (may be y)
+};
+cudaError_t gemv_launch_fused(int type, const uint8_t *W, float *y, int64_t N, int64_t K, int M, const GemvFusion &f,
+                              unsigned *status, int num_sms, bool pdl, cudaStream_t stream);
+
 // ---------------------------------------------------------------- prefill GEMM (gemm_tc.cu)
 
 // Launches the tcgen05 kernel for any M >= 1. Returns cudaErrorNotSupported when the shape

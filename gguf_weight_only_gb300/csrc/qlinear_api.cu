@@ -146,6 +146,25 @@ int run_multi(int type, int n_proj, const void *const *W, const int64_t *N, int6
     return e == cudaSuccess ? QL_OK : cuda_fail(e);
 }
 
+bool misaligned(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; }
+
+// A decode launch with a fused prologue (SiLU-gated or RMSNorm x) and optional residual.
+int run_fused(int type, const void *W, int64_t N, int64_t K, int64_t M, const ql::GemvFusion &f, const void *a,
+              const void *b, float *y, void *stream) {
+    int rc = validate(type, W, N, K, a, M, y);   // a: the [M, K] input that stands in for x
+    if (rc != QL_OK) return rc;
+    if (!b) return QL_ERR_NULL;
+    if (misaligned(b) || (f.residual && misaligned(f.residual)) || (f.xnorm && misaligned(f.xnorm))) return QL_ERR_ALIGN;
+    if (!(f.eps >= 0.f) || f.eps > 3.0e38f) return QL_ERR_SHAPE;   // also rejects NaN
+    if (M > ql::kGemvMaxM) return QL_ERR_UNSUPPORTED;
+    DeviceState *s = nullptr;
+    if ((rc = device_state(&s)) != QL_OK) return rc;
+    cudaError_t e = ql::gemv_launch_fused(type, static_cast<const uint8_t *>(W), y, N, K, static_cast<int>(M), f,
+                                          s->status_word, s->num_sms, s->pdl, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return QL_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? QL_OK : cuda_fail(e);
+}
+
 }  // namespace
 
 extern "C" {
@@ -171,6 +190,28 @@ int qlinear_multi(int type, int n_proj, const void *const *W_blocks, const int64
 }
 
 int qlinear_max_projections(void) { return ql::kGemvMaxProj; }
+
+int qlinear_silu_mul(int type, const void *W_blocks, int64_t N, int64_t K, const void *gate_fp16, const float *up_fp32,
+                     int64_t M, const float *residual, float *y_fp32, void *stream) {
+    ql::GemvFusion f;
+    f.pro = 1;
+    f.gate = static_cast<const __half *>(gate_fp16);
+    f.up_or_h = up_fp32;
+    f.residual = residual;
+    return run_fused(type, W_blocks, N, K, M, f, gate_fp16, up_fp32, y_fp32, stream);
+}
+
+int qlinear_rmsnorm(int type, const void *W_blocks, int64_t N, int64_t K, const float *h_fp32, const float *norm_w_fp32,
+                    float eps, int64_t M, const float *residual, float *y_fp32, void *xnorm_fp16, void *stream) {
+    ql::GemvFusion f;
+    f.pro = 2;
+    f.up_or_h = h_fp32;
+    f.norm_w = norm_w_fp32;
+    f.eps = eps;
+    f.xnorm = static_cast<__half *>(xnorm_fp16);
+    f.residual = residual;
+    return run_fused(type, W_blocks, N, K, M, f, h_fp32, norm_w_fp32, y_fp32, stream);
+}
 
 int qlinear_block_bytes(int type) {
     const int b = ql::block_bytes_of(type);

@@ -110,6 +110,32 @@ int qlinear_multi(int type, int n_proj, const void *const *W_blocks, const int64
 /* Most projections one qlinear_multi() call takes (4). */
 int qlinear_max_projections(void);
 
+/*
+ * Decode calls with the layer's input produced inside the launch (fused prologue) and an
+ * optional residual added to the output (fused epilogue). The pages fuse both element-wise
+ * producers into the consuming linear and check the result equals the separate steps
+ * (test/unit/test_llm_quant_cpu.py: test_q8_silu_linear_matches_separate,
+ * test_f16_linear_matches_standard).
+ *
+ * qlinear_silu_mul: y = x . dequant(W)^T (+ residual) with x = fp16(silu(gate) * up),
+ *   silu(g) = g / (1 + e^-g), evaluated in fp32 and rounded once to fp16 (the pages'
+ *   silu_mul(gate, up).half()). gate_fp16: [M, K] binary16; up_fp32: [M, K] fp32.
+ * qlinear_rmsnorm: y = x . dequant(W)^T (+ residual) with
+ *   x = fp16(h * rsqrt(mean_k(h^2) + eps) * norm_w), h_fp32 [M, K], norm_w_fp32 [K], eps >= 0,
+ *   evaluated in fp32. When xnorm_fp16 is not NULL the fp16 x is also written there ([M, K]).
+ * Both: M <= qlinear_gemv_max_m() (else QL_ERR_UNSUPPORTED); residual is NULL or an [M, N]
+ * fp32 array, and may be y_fp32 itself (y += x . W^T). Device pointers are 16-byte aligned
+ * (QL_ERR_ALIGN); W, gate/h, up/norm_w and y must not be NULL (QL_ERR_NULL); a negative or
+ * non-finite eps gives QL_ERR_SHAPE. Validation, ownership and streams as for qlinear().
+ * The result matches the oracle within the layer's tolerance widened by one fp16 rounding
+ * step of each activation (the fp32 prologue may round across a boundary the fp64 one does not).
+ */
+int qlinear_silu_mul(int type, const void *W_blocks, int64_t N, int64_t K, const void *gate_fp16,
+                     const float *up_fp32, int64_t M, const float *residual, float *y_fp32, void *stream);
+int qlinear_rmsnorm(int type, const void *W_blocks, int64_t N, int64_t K, const float *h_fp32,
+                    const float *norm_w_fp32, float eps, int64_t M, const float *residual, float *y_fp32,
+                    void *xnorm_fp16, void *stream);
+
 /* Bytes per 256-weight superblock of `type` (144/176/210/136), or QL_ERR_TYPE. */
 int qlinear_block_bytes(int type);
 

@@ -125,3 +125,38 @@ MULTI_BAD = [
 def test_multi_bad_arguments_rejected_before_launch(lib, case):
     t, W, N, K, x, M, y, n, expect = case
     assert _multi(lib, t, W, N, K, x, M, y, n) == expect
+
+
+# ------------------------------------------------------------------ fused prologues
+
+FUSED_BAD = [
+    # (fn, type, W, N, K, a, b, M, residual, y, extra(eps, xnorm), expected)
+    ("silu", 7, 16, 8, 256, 16, 32, 1, 0, 48, None, -1),
+    ("silu", 12, 16, 8, 300, 16, 32, 1, 0, 48, None, -2),
+    ("silu", 12, 16, 8, 256, 16, 32, 0, 0, 48, None, -2),
+    ("silu", 12, 0, 8, 256, 16, 32, 1, 0, 48, None, -3),
+    ("silu", 12, 16, 8, 256, 0, 32, 1, 0, 48, None, -3),
+    ("silu", 12, 16, 8, 256, 16, 0, 1, 0, 48, None, -3),
+    ("silu", 12, 16, 8, 256, 16, 32, 1, 0, 0, None, -3),
+    ("silu", 12, 16, 8, 256, 24, 32, 1, 0, 48, None, -4),
+    ("silu", 12, 16, 8, 256, 16, 40, 1, 0, 48, None, -4),
+    ("silu", 12, 16, 8, 256, 16, 32, 1, 72, 48, None, -4),
+    ("silu", 12, 16, 8, 256, 16, 32, 9, 0, 48, None, -7),
+    ("rms", 12, 16, 8, 256, 16, 32, 1, 0, 48, (-1.0, 0), -2),
+    ("rms", 12, 16, 8, 256, 16, 32, 1, 0, 48, (float("nan"), 0), -2),
+    ("rms", 12, 16, 8, 256, 16, 0, 1, 0, 48, (1e-6, 0), -3),
+    ("rms", 12, 16, 8, 256, 16, 32, 1, 0, 48, (1e-6, 88), -4),
+    ("rms", 12, 16, 8, 256, 16, 32, 9, 0, 48, (1e-6, 0), -7),
+]
+
+
+@pytest.mark.parametrize("case", FUSED_BAD)
+def test_fused_bad_arguments_rejected_before_launch(lib, case):
+    fn, t, W, N, K, a, b, M, r, y, extra, expect = case
+    v = lambda p: ctypes.c_void_p(p or None)
+    if fn == "silu":
+        rc = lib.qlinear_silu_mul(t, v(W), N, K, v(a), v(b), M, v(r), v(y), None)
+    else:
+        eps, xn = extra
+        rc = lib.qlinear_rmsnorm(t, v(W), N, K, v(a), v(b), eps, M, v(r), v(y), v(xn), None)
+    assert rc == expect

@@ -435,6 +435,52 @@ def time_fused(kind, t, K, N, M, reps, dev, stream, l2, lib, replays=5):
     return float(np.median(times))
 
 
+def time_argmax(t, K, N, M, reps, dev, stream, l2, lib, replays=5):
+    """As time_shape, for the greedy head (qlinear_argmax: a memset and two kernels per call).
+    Returns ms per call."""
+    import torch
+    wb = N * (K // 256) * BB[t]
+    Pk = max(2, int(np.ceil(2.2 * l2 / wb)))
+    W0 = torch.from_numpy(synth.weights(t, N, K, [7, t, K, N])).to(dev)
+    Wk = [W0.clone() for _ in range(Pk)]
+    x = torch.from_numpy(synth.activations(M, K, [8, t, M])).to(dev)
+    idx = torch.empty(M, dtype=torch.int64, device=dev)
+    val = torch.empty(M, dtype=torch.float32, device=dev)
+    sh = stream.cuda_stream
+
+    def call(i):
+        rc = lib.qlinear_argmax(t, Wk[i % Pk].data_ptr(), N, K, x.data_ptr(), M, idx.data_ptr(), val.data_ptr(), sh)
+        if rc != 0:
+            raise RuntimeError(f"qlinear_argmax failed: {rc}")
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            call(i)
+    torch.cuda.synchronize(dev)
+    gk = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gk, stream=stream):
+        for i in range(reps):
+            call(i)
+    with torch.cuda.stream(stream):
+        gk.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for _ in range(replays):
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            gk.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(e0.elapsed_time(e1) / reps)
+    del gk, Wk
+    torch.cuda.empty_cache()
+    return float(np.median(times))
+
+
+# Greedy output heads: type, K, N (vocabulary), M
+TABLE_HEAD = [(14, 4096, 151936, 1), (14, 4096, 32000, 1)]
+
 # Fused decode calls: kind, type, K, N, M (the 8B down projection fed by the SiLU gate, the
 # 8B gate projection fed by RMSNorm)
 TABLE_FUSED = [("silu", 12, 12288, 4096, 1), ("rmsnorm", 12, 4096, 12288, 1)]
@@ -493,6 +539,14 @@ def run_table(args):
                                                      "frac": round(byts / (ms * 1e-3) / 1e9 / hbm, 4)}
         print(json.dumps({"projections": name, "type": TYPE_NAMES[t], "K": K, "N": list(Ns), "M": M, **res,
                           "peak_kind": peak_kind, "status": ql.device_status()}), flush=True)
+    for t, K, N, M in TABLE_HEAD:
+        ms = time_argmax(t, K, N, M, 50, dev, stream, l2, lib)
+        plain = time_shape(t, K, N, M, lib.qlinear, 50, dev, stream, l2, replays=5)
+        byts = N * (K // 256) * BB[t] + 2 * M * K + 12 * M
+        print(json.dumps({"argmax_head": TYPE_NAMES[t], "K": K, "N": N, "M": M, "us": round(ms * 1e3, 2),
+                          "GBs": round(byts / (ms * 1e-3) / 1e9, 1), "frac": round(byts / (ms * 1e-3) / 1e9 / hbm, 4),
+                          "logits_us": round(plain * 1e3, 2), "peak_kind": peak_kind,
+                          "status": ql.device_status()}), flush=True)
     for kind, t, K, N, M in TABLE_FUSED:
         ms = time_fused(kind, t, K, N, M, 200, dev, stream, l2, lib)
         plain = time_shape(t, K, N, M, lib.qlinear, 200, dev, stream, l2, replays=5)

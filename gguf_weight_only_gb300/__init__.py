@@ -18,13 +18,14 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libqlinear.so")
 
 Q4_K, Q5_K, Q6_K, IQ4_XS = 12, 13, 14, 23
 STATUS = {0: "QL_OK", -1: "QL_ERR_TYPE", -2: "QL_ERR_SHAPE", -3: "QL_ERR_NULL", -4: "QL_ERR_ALIGN",
-          -5: "QL_ERR_CUDA", -6: "QL_ERR_TIMEOUT", -7: "QL_ERR_UNSUPPORTED", -8: "QL_ERR_DEVICE"}
+          -5: "QL_ERR_CUDA", -6: "QL_ERR_TIMEOUT", -7: "QL_ERR_UNSUPPORTED", -8: "QL_ERR_DEVICE",
+          -9: "QL_ERR_INDEX"}
 # Every function include/qlinear.h declares (the symbol-export test checks this list
 # against the header).
 EXPORTS = ("qlinear", "qlinear_gemv", "qlinear_gemm", "qlinear_block_bytes", "qlinear_gemv_max_m",
            "qlinear_strerror", "qlinear_last_cuda_error", "qlinear_device_status", "qlinear_launch_count",
            "qlinear_selftest_wait_timeout", "qlinear_multi", "qlinear_max_projections", "qlinear_silu_mul",
-           "qlinear_rmsnorm")
+           "qlinear_rmsnorm", "qlinear_argmax", "qlinear_embed")
 
 _lib = None
 
@@ -70,6 +71,10 @@ def lib() -> ctypes.CDLL:
         l.qlinear_silu_mul.restype = ctypes.c_int
         l.qlinear_rmsnorm.argtypes = [ctypes.c_int, vp, i64, i64, vp, vp, ctypes.c_float, i64, vp, vp, vp, vp]
         l.qlinear_rmsnorm.restype = ctypes.c_int
+        l.qlinear_argmax.argtypes = [ctypes.c_int, vp, i64, i64, vp, i64, vp, vp, vp]
+        l.qlinear_argmax.restype = ctypes.c_int
+        l.qlinear_embed.argtypes = [ctypes.c_int, vp, i64, i64, vp, i64, vp, ctypes.c_int, vp]
+        l.qlinear_embed.restype = ctypes.c_int
         _lib = l
     return _lib
 
@@ -244,6 +249,47 @@ def qlinear_rmsnorm(W, ggml_type: int, N: int, K: int, h, norm_w, eps: float, re
                                  float(eps), M, residual.data_ptr() if residual is not None else None, out.data_ptr(),
                                  xnorm.data_ptr() if xnorm is not None else None, _stream_handle(stream)),
            "qlinear_rmsnorm")
+    return out
+
+
+def _weights(W, ggml_type, N, K):
+    import torch
+    if not (isinstance(W, torch.Tensor) and W.is_cuda and W.dtype == torch.uint8 and W.is_contiguous()):
+        raise TypeError("W must be a contiguous uint8 CUDA tensor")
+    bb = block_bytes(ggml_type)
+    if bb > 0 and W.numel() < N * (K // 256) * bb:
+        raise ValueError("W holds fewer bytes than N*K/256 superblocks")
+
+
+def qlinear_argmax(W, ggml_type: int, N: int, K: int, x, stream=None):
+    """Greedy output head for M <= 8 tokens: (index int64 [M], value float32 [M]) of the first
+    largest y[m, :] of x . dequant(W)^T, without materialising y."""
+    import torch
+    M = x.shape[0] if x.dim() == 2 else 1
+    _mk(x, torch.float16, (M, K), "x")
+    _weights(W, ggml_type, N, K)
+    idx = torch.empty(M, dtype=torch.int64, device=x.device)
+    val = torch.empty(M, dtype=torch.float32, device=x.device)
+    _check(lib().qlinear_argmax(int(ggml_type), W.data_ptr(), int(N), int(K), x.data_ptr(), M, idx.data_ptr(),
+                                val.data_ptr(), _stream_handle(stream)), "qlinear_argmax")
+    return idx, val
+
+
+def qlinear_embed(W, ggml_type: int, N: int, K: int, ids, fp16: bool = False, out=None, stream=None):
+    """Embedding gather: out[m, :] = dequant(W)[ids[m], :] (ids: int32 CUDA tensor), each weight
+    rounded once to fp32 (or fp16)."""
+    import torch
+    if not (isinstance(ids, torch.Tensor) and ids.is_cuda and ids.dtype == torch.int32 and ids.is_contiguous()):
+        raise TypeError("ids must be a contiguous int32 CUDA tensor")
+    M = ids.numel()
+    _weights(W, ggml_type, N, K)
+    dt = torch.float16 if fp16 else torch.float32
+    if out is None:
+        out = torch.empty((M, K), dtype=dt, device=ids.device)
+    else:
+        _mk(out, dt, (M, K), "out")
+    _check(lib().qlinear_embed(int(ggml_type), W.data_ptr(), int(N), int(K), ids.data_ptr(), M, out.data_ptr(),
+                               1 if fp16 else 0, _stream_handle(stream)), "qlinear_embed")
     return out
 
 

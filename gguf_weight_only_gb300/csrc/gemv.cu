@@ -89,6 +89,7 @@ struct GemvArgs {
     float eps;
     __half *xnorm;           // pro 2: optional [M, K] output of the normalised activations
     const float *residual;   // optional [M, N] added to y (single projection); may be y itself
+    unsigned long long *best;  // greedy head: per token the largest packed (value, row) key, zeroed by the host
     int K, M, nsb;
     int S;                   // superblocks per stage
     int kw;                  // superblocks of the K slice each warp owns
@@ -420,6 +421,16 @@ __device__ __forceinline__ void superblock_iq4(uint32_t blk_a, uint32_t blk_b, c
 // Shared-memory scratch of the RMSNorm prologue, in the free tail of the first (barrier)
 // kilobyte: per-warp partial sums of h^2 for each token.
 constexpr uint32_t kSqOffset = 512;
+// ... and of the greedy-head epilogue: per-warp best keys of one token.
+constexpr uint32_t kArgOffset = 832;
+
+// Key whose unsigned order is (value, then the smaller row): the float's bits made monotonic
+// (+0 and -0 made equal), then the row counted down from 2^32 - 1.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int row) {
+    const uint32_t bits = (v == 0.f) ? 0u : __float_as_uint(v);
+    const uint32_t ord = (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+    return (static_cast<unsigned long long>(ord) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(row));
+}
 
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
     const __half2 h = __floats2half2_rn(a, b);
@@ -488,7 +499,7 @@ constexpr int kFillGroup = 4;
 // next unit as soon as it has consumed it, across tile boundaries. The warps' 16 x 8 partial
 // tiles go to shared memory; after each round of tiles they are summed in fixed order.
 
-template <int TYPE, bool TMA, bool XRES, bool MULTI, bool PRO>
+template <int TYPE, bool TMA, bool XRES, bool MULTI, bool PRO, bool ARGMAX>
 __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const __grid_constant__ GemvMaps wmaps,
                                                       const __grid_constant__ CUtensorMap xmap,
                                                       const __grid_constant__ GemvArgs p) {
@@ -787,17 +798,45 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
       // end of the round: each tile's partials summed over its K slices in fixed order
       __syncthreads();
       const int per_tile = 16 * p.M;
-      for (int q = threadIdx.x; q < (rend - round0) * per_tile; q += blockDim.x) {
-          const int tt = q / per_tile, rem = q - tt * per_tile;   // tile of the round, token * 16 + row
-          const float *src = red + tt * p.ks * per_tile + rem;
-          float sum = 0.f;
-          for (int kk = 0; kk < p.ks; ++kk) sum += src[kk * per_tile];
-          int jp;
-          const int row = tile_rows(round0 + tt, jp) + (rem & 15);
-          if (row < p.N[jp]) {
-              const int64_t o = static_cast<int64_t>(rem >> 4) * p.N[jp] + row;
-              if constexpr (PRO) p.y[jp][o] = p.residual ? sum + p.residual[o] : sum;   // y may be the residual
-              else p.y[jp][o] = sum;
+      if constexpr (ARGMAX) {
+          // greedy head: per token, the CTA's best (value, row) key, then one atomic max;
+          // each value is summed exactly as the y path sums it
+          unsigned long long *wbest = reinterpret_cast<unsigned long long *>(gbase + kArgOffset);
+          for (int m = 0; m < p.M; ++m) {
+              unsigned long long bk = 0ull;
+              for (int q = threadIdx.x; q < (rend - round0) * 16; q += blockDim.x) {
+                  const int tt = q >> 4;
+                  const float *src = red + tt * p.ks * per_tile + m * 16 + (q & 15);
+                  float sum = 0.f;
+                  for (int kk = 0; kk < p.ks; ++kk) sum += src[kk * per_tile];
+                  int jp;
+                  const int row = tile_rows(round0 + tt, jp) + (q & 15);
+                  if (row < p.N[0]) bk = max(bk, argmax_key(sum, row));
+              }
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) bk = max(bk, __shfl_xor_sync(0xFFFFFFFFu, bk, o));
+              if (lane == 0) wbest[warp] = bk;
+              __syncthreads();
+              if (threadIdx.x == 0) {
+                  unsigned long long cb = 0ull;
+                  for (int w2 = 0; w2 < static_cast<int>(blockDim.x >> 5); ++w2) cb = max(cb, wbest[w2]);
+                  atomicMax(p.best + m, cb);
+              }
+              __syncthreads();
+          }
+      } else {
+          for (int q = threadIdx.x; q < (rend - round0) * per_tile; q += blockDim.x) {
+              const int tt = q / per_tile, rem = q - tt * per_tile;   // tile of the round, token * 16 + row
+              const float *src = red + tt * p.ks * per_tile + rem;
+              float sum = 0.f;
+              for (int kk = 0; kk < p.ks; ++kk) sum += src[kk * per_tile];
+              int jp;
+              const int row = tile_rows(round0 + tt, jp) + (rem & 15);
+              if (row < p.N[jp]) {
+                  const int64_t o = static_cast<int64_t>(rem >> 4) * p.N[jp] + row;
+                  if constexpr (PRO) p.y[jp][o] = p.residual ? sum + p.residual[o] : sum;   // y may be the residual
+                  else p.y[jp][o] = sum;
+              }
           }
       }
       if (rend < ntiles) __syncthreads();   // the next round reuses the slots
@@ -919,10 +958,10 @@ GemvPlan make_plan(int type, int64_t T, int64_t K, int M, int num_sms, bool need
     return pl;
 }
 
-template <int TYPE, bool TMA, bool XRES, bool MULTI, bool PRO = false>
+template <int TYPE, bool TMA, bool XRES, bool MULTI, bool PRO = false, bool ARGMAX = false>
 cudaError_t launch_t(const GemvMaps &wm, const CUtensorMap &xm, const GemvArgs &a, int grid, int threads,
                      size_t smem, bool pdl, cudaStream_t st) {
-    auto kern = gemv_kernel<TYPE, TMA, XRES, MULTI, PRO>;
+    auto kern = gemv_kernel<TYPE, TMA, XRES, MULTI, PRO, ARGMAX>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -938,6 +977,11 @@ cudaError_t launch_t(const GemvMaps &wm, const CUtensorMap &xm, const GemvArgs &
 template <int TYPE>
 cudaError_t launch_type(bool tma, bool xres, const GemvMaps &wm, const CUtensorMap &xm, const GemvArgs &a,
                         int grid, int threads, size_t smem, bool pdl, cudaStream_t st) {
+    if (a.best) {   // greedy head: one projection, x resident (the plan guarantees it)
+        if (a.nproj != 1 || !xres || a.pro != 0) return cudaErrorInvalidValue;
+        return tma ? launch_t<TYPE, true, true, false, false, true>(wm, xm, a, grid, threads, smem, pdl, st)
+                   : launch_t<TYPE, false, true, false, false, true>(wm, xm, a, grid, threads, smem, pdl, st);
+    }
     if (a.pro != 0) {   // fused prologues: one projection, x resident (the plan guarantees it)
         if (a.nproj != 1 || !xres) return cudaErrorInvalidValue;
         return tma ? launch_t<TYPE, true, true, false, true>(wm, xm, a, grid, threads, smem, pdl, st)
@@ -964,7 +1008,9 @@ cudaError_t launch_impl(int type, int nproj, const GemvProj *proj, const __half 
     const int bb = block_bytes_of(type);
     if (bb < 0 || M < 1 || M > kGemvMaxM || nproj < 1 || nproj > kGemvMaxProj) return cudaErrorInvalidValue;
     const int pro = fu ? fu->pro : 0;
-    if (pro < 0 || pro > 2 || (fu && fu->residual && nproj != 1)) return cudaErrorInvalidValue;
+    const bool head = fu && fu->best;
+    if (pro < 0 || pro > 2 || (fu && (fu->residual || fu->best) && nproj != 1) || (head && pro != 0))
+        return cudaErrorInvalidValue;
     int tile0[kGemvMaxProj + 1];
     int64_t T = 0;
     for (int j = 0; j < nproj; ++j) {
@@ -973,7 +1019,7 @@ cudaError_t launch_impl(int type, int nproj, const GemvProj *proj, const __half 
         if (T > (int64_t(1) << 30)) return cudaErrorInvalidValue;
     }
     tile0[nproj] = static_cast<int>(T);
-    GemvPlan pl = make_plan(type, T, K, M, num_sms, pro != 0);
+    GemvPlan pl = make_plan(type, T, K, M, num_sms, pro != 0 || head);
     if (pl.smem > 227 * 1024) return cudaErrorNotSupported;
     const int64_t row_bytes = K / 256 * bb;
     for (int j = 0; j <= nproj; ++j) pl.a.tile0[j] = tile0[j];
@@ -994,6 +1040,7 @@ cudaError_t launch_impl(int type, int nproj, const GemvProj *proj, const __half 
         pl.a.eps = fu->eps;
         pl.a.xnorm = fu->xnorm;
         pl.a.residual = fu->residual;
+        pl.a.best = fu->best;
     }
     GemvMaps wm{};
     CUtensorMap xm{};
@@ -1039,6 +1086,38 @@ cudaError_t gemv_launch_fused(int type, const uint8_t *W, float *y, int64_t N, i
                               unsigned *status, int num_sms, bool pdl, cudaStream_t stream) {
     const GemvProj one{W, y, N};
     return launch_impl(type, 1, &one, nullptr, K, M, &f, status, num_sms, pdl, stream);
+}
+
+namespace {
+
+// Packed keys -> row (in place, as int64) and value.
+__global__ void argmax_finalize_kernel(unsigned long long *keys, float *val, int M) {
+    const int m = threadIdx.x;
+    if (m < M) {
+        const unsigned long long k = keys[m];
+        const uint32_t ord = static_cast<uint32_t>(k >> 32);
+        const uint32_t bits = (ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord;
+        if (val) val[m] = __uint_as_float(bits);
+        reinterpret_cast<long long *>(keys)[m] = static_cast<long long>(0xFFFFFFFFu - static_cast<uint32_t>(k));
+    }
+}
+
+}  // namespace
+
+cudaError_t gemv_launch_argmax(int type, const uint8_t *W, int64_t N, int64_t K, const __half *x, int M,
+                               long long *index_out, float *value_out, unsigned *status, int num_sms, cudaStream_t stream) {
+    if (M < 1 || M > kGemvMaxM) return cudaErrorInvalidValue;
+    unsigned long long *keys = reinterpret_cast<unsigned long long *>(index_out);
+    cudaError_t e = cudaMemsetAsync(keys, 0, static_cast<size_t>(M) * sizeof(unsigned long long), stream);
+    if (e != cudaSuccess) return e;
+    GemvFusion f;
+    f.best = keys;
+    const GemvProj one{W, nullptr, N};
+    // launched in full stream order (no early start): the keys must be zero before any atomic
+    e = launch_impl(type, 1, &one, x, K, M, &f, status, num_sms, false, stream);
+    if (e != cudaSuccess) return e;
+    argmax_finalize_kernel<<<1, 32, 0, stream>>>(keys, value_out, M);
+    return cudaGetLastError();
 }
 
 }  // namespace ql

@@ -45,9 +45,16 @@ struct GemvFusion {
     float eps = 0.f;                 // pro 2
     __half *xnorm = nullptr;         // pro 2: optional [M, K] copy of the fp16 normalised x
     const float *residual = nullptr; // optional [M, N], added to y (may be y)
+    unsigned long long *best = nullptr;  // greedy head: per-token packed keys (zeroed), y not written
 };
 cudaError_t gemv_launch_fused(int type, const uint8_t *W, float *y, int64_t N, int64_t K, int M, const GemvFusion &f,
                               unsigned *status, int num_sms, bool pdl, cudaStream_t stream);
+
+// Greedy output head: index_out[m] = the first n with the largest y[m, n] (int64), value_out[m]
+// (optional) = that y, without writing y. index_out serves as the packed-key scratch: it is
+// zeroed, reduced into by atomic max from every CTA, then rewritten by a one-warp kernel.
+cudaError_t gemv_launch_argmax(int type, const uint8_t *W, int64_t N, int64_t K, const __half *x, int M,
+                               long long *index_out, float *value_out, unsigned *status, int num_sms, cudaStream_t stream);
 
 // ---------------------------------------------------------------- prefill GEMM (gemm_tc.cu)
 
@@ -56,6 +63,14 @@ cudaError_t gemv_launch_fused(int type, const uint8_t *W, float *y, int64_t N, i
 cudaError_t gemm_launch(int type, const uint8_t *W, const __half *x, float *y, int64_t N, int64_t K, int64_t M,
                         unsigned *status, int num_sms, bool pdl, cudaStream_t stream);
 int gemm_launch_count(int type, int64_t N, int64_t K, int64_t M);
+
+// ---------------------------------------------------------------- embedding gather (embed.cu)
+
+// out[m, :] = dequant(W)[ids[m], :], the exact weights rounded once to fp32 (or fp16 with
+// half_out); an id outside [0, N) gives a zero row and sets kStatusBadIndex in *status.
+cudaError_t embed_launch(int type, const uint8_t *W, const int32_t *ids, int64_t N, int64_t K, int64_t M, void *out,
+                         bool half_out, unsigned *status, cudaStream_t stream);
+int embed_launch_count(int64_t M);
 
 // ---------------------------------------------------------------- tensor maps (tmap.cu)
 

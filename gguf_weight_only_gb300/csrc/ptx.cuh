@@ -15,7 +15,7 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 }
 
 // Device-side status bits (OR-ed into the word the host passes to every kernel).
-enum : uint32_t { kStatusTimeout = 1u };
+enum : uint32_t { kStatusTimeout = 1u, kStatusBadIndex = 2u };
 
 
 // ---------------------------------------------------------------- mbarrier

@@ -191,6 +191,38 @@ int qlinear_multi(int type, int n_proj, const void *const *W_blocks, const int64
 
 int qlinear_max_projections(void) { return ql::kGemvMaxProj; }
 
+int qlinear_argmax(int type, const void *W_blocks, int64_t N, int64_t K, const void *x_fp16, int64_t M,
+                   int64_t *index_out, float *value_out, void *stream) {
+    int rc = validate(type, W_blocks, N, K, x_fp16, M, reinterpret_cast<const float *>(index_out));
+    if (rc != QL_OK) return rc;
+    if (value_out && misaligned(value_out)) return QL_ERR_ALIGN;
+    if (M > ql::kGemvMaxM) return QL_ERR_UNSUPPORTED;
+    DeviceState *s = nullptr;
+    if ((rc = device_state(&s)) != QL_OK) return rc;
+    cudaError_t e = ql::gemv_launch_argmax(type, static_cast<const uint8_t *>(W_blocks), N, K,
+                                           static_cast<const __half *>(x_fp16), static_cast<int>(M),
+                                           reinterpret_cast<long long *>(index_out), value_out, s->status_word,
+                                           s->num_sms, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return QL_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? QL_OK : cuda_fail(e);
+}
+
+int qlinear_embed(int type, const void *W_blocks, int64_t N, int64_t K, const int32_t *ids, int64_t M, void *out,
+                  int out_fp16, void *stream) {
+    if (ql::block_bytes_of(type) < 0) return QL_ERR_TYPE;
+    if (N < 1 || M < 1 || K < 256 || K % 256 != 0 || N > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 24) ||
+        M > (int64_t(1) << 30))
+        return QL_ERR_SHAPE;
+    if (!W_blocks || !ids || !out) return QL_ERR_NULL;
+    if (misaligned(W_blocks) || misaligned(out) || (reinterpret_cast<uintptr_t>(ids) & 3u)) return QL_ERR_ALIGN;
+    DeviceState *s = nullptr;
+    int rc = device_state(&s);
+    if (rc != QL_OK) return rc;
+    cudaError_t e = ql::embed_launch(type, static_cast<const uint8_t *>(W_blocks), ids, N, K, M, out, out_fp16 != 0,
+                                     s->status_word, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QL_OK : cuda_fail(e);
+}
+
 int qlinear_silu_mul(int type, const void *W_blocks, int64_t N, int64_t K, const void *gate_fp16, const float *up_fp32,
                      int64_t M, const float *residual, float *y_fp32, void *stream) {
     ql::GemvFusion f;
@@ -231,6 +263,7 @@ const char *qlinear_strerror(int status) {
     case QL_ERR_TIMEOUT: return "a device-side bounded wait ran out";
     case QL_ERR_UNSUPPORTED: return "the requested kernel cannot run this shape";
     case QL_ERR_DEVICE: return "current device is not an sm_103 (GB300) GPU";
+    case QL_ERR_INDEX: return "an index read on the device was out of range (embedding id)";
     default: return "unknown status";
     }
 }
@@ -255,7 +288,8 @@ int qlinear_device_status(void *stream) {
     unsigned word = 0, zero = 0;
     if ((e = cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word))) != cudaSuccess) return cuda_fail(e);
     if (word != 0 && (e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero))) != cudaSuccess) return cuda_fail(e);
-    return word ? QL_ERR_TIMEOUT : QL_OK;
+    if (word & ql::kStatusTimeout) return QL_ERR_TIMEOUT;
+    return word ? QL_ERR_INDEX : QL_OK;
 }
 
 int qlinear_launch_count(int type, int64_t N, int64_t K, int64_t M) {

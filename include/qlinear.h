@@ -62,7 +62,8 @@ typedef enum {
     QL_ERR_CUDA = -5,        /* a CUDA runtime call or kernel launch failed */
     QL_ERR_TIMEOUT = -6,     /* a device-side bounded wait ran out (see qlinear_device_status) */
     QL_ERR_UNSUPPORTED = -7, /* the forced path cannot run this shape on this device */
-    QL_ERR_DEVICE = -8       /* the current device is not an sm_103 (GB300) part */
+    QL_ERR_DEVICE = -8,      /* the current device is not an sm_103 (GB300) part */
+    QL_ERR_INDEX = -9        /* an index read on the device was out of range (see qlinear_embed) */
 } ql_status;
 
 /*
@@ -130,6 +131,34 @@ int qlinear_max_projections(void);
  * The result matches the oracle within the layer's tolerance widened by one fp16 rounding
  * step of each activation (the fp32 prologue may round across a boundary the fp64 one does not).
  */
+/*
+ * qlinear_argmax: the greedy output head. For each token m < M (M <= qlinear_gemv_max_m()),
+ * index_out[m] = the first n with the largest y[m][n] of y = x . dequant(W)^T, and, when
+ * value_out is not NULL, value_out[m] = that y (fp32), without materialising y: the decode
+ * kernel keeps, per CTA and token, the best (value, row) and merges it across CTAs by one
+ * 64-bit atomic maximum. Every y[m][n] is the value qlinear() computes for it, bit for bit, so
+ * the choice equals the first maximum of qlinear()'s output (+0 and -0 compare equal; a NaN
+ * ranks above every number). The pages pick the next token from a Q6_K head this way and check
+ * it against the argmax of the materialised logits (test/unit/test_llm_quant_cpu.py,
+ * test_q6_argmax_matches_materialized_logits).
+ * index_out: M int64 (16-byte aligned), also used as scratch; value_out: M floats or NULL.
+ * Enqueues a memset and two kernels on `stream`. Other arguments as for qlinear().
+ */
+int qlinear_argmax(int type, const void *W_blocks, int64_t N, int64_t K, const void *x_fp16, int64_t M,
+                   int64_t *index_out, float *value_out, void *stream);
+
+/*
+ * qlinear_embed: the embedding gather, out[m][k] = dequant(W)[ids[m]][k] for m < M, k < K:
+ * each weight is its exact value rounded once to fp32 (out_fp16 == 0) or to fp16, round to
+ * nearest even (out_fp16 != 0). The pages' quantized Embedding returns the fp16 rounding of the
+ * dequantised rows (test/unit/test_llm_quant_cpu.py, test_q4_embedding_matches_reference).
+ * W_blocks: N rows as for qlinear(); ids: M int32 device indices (4-byte aligned); out: M*K
+ * elements (16-byte aligned). An id outside [0, N) cannot be checked on the host: its row is
+ * written as zeros and the next qlinear_device_status() reports QL_ERR_INDEX.
+ */
+int qlinear_embed(int type, const void *W_blocks, int64_t N, int64_t K, const int32_t *ids, int64_t M, void *out,
+                  int out_fp16, void *stream);
+
 int qlinear_silu_mul(int type, const void *W_blocks, int64_t N, int64_t K, const void *gate_fp16,
                      const float *up_fp32, int64_t M, const float *residual, float *y_fp32, void *stream);
 int qlinear_rmsnorm(int type, const void *W_blocks, int64_t N, int64_t K, const float *h_fp32,
@@ -150,7 +179,8 @@ int qlinear_last_cuda_error(void);
 
 /* Synchronises `stream`, then reads and clears the device status word of the current
  * device: QL_OK, QL_ERR_TIMEOUT if a bounded wait in a kernel ran out since the last
- * check, or QL_ERR_CUDA if the synchronisation itself failed. */
+ * check, QL_ERR_INDEX if an embedding id was out of range (and no wait ran out), or
+ * QL_ERR_CUDA if the synchronisation itself failed. */
 int qlinear_device_status(void *stream);
 
 /* Number of kernels one qlinear() call of this shape launches (for launch accounting);

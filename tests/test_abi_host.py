@@ -43,8 +43,8 @@ def test_block_bytes_and_metadata(lib):
     assert [ql.block_bytes(t) for t in (12, 13, 14, 23)] == [144, 176, 210, 136]
     assert ql.block_bytes(2) == -1
     assert ql.gemv_max_m() == 8
-    for s in range(-8, 1):
-        assert isinstance(ql.strerror(s), str) and ql.strerror(s)
+    for s in range(-9, 1):
+        assert isinstance(ql.strerror(s), str) and ql.strerror(s) != "unknown status"
     assert ql.strerror(-99) == "unknown status"
     assert lib.qlinear_last_cuda_error() == 0
 
@@ -160,3 +160,49 @@ def test_fused_bad_arguments_rejected_before_launch(lib, case):
         eps, xn = extra
         rc = lib.qlinear_rmsnorm(t, v(W), N, K, v(a), v(b), eps, M, v(r), v(y), v(xn), None)
     assert rc == expect
+
+
+# ------------------------------------------------------------------ greedy head and embedding gather
+
+HEAD_BAD = [
+    # (type, W, N, K, x, M, index_out, value_out, expected)
+    (7, 16, 8, 256, 16, 1, 32, 48, -1),
+    (12, 16, 8, 300, 16, 1, 32, 48, -2),
+    (12, 16, 0, 256, 16, 1, 32, 48, -2),
+    (12, 0, 8, 256, 16, 1, 32, 48, -3),
+    (12, 16, 8, 256, 0, 1, 32, 48, -3),
+    (12, 16, 8, 256, 16, 1, 0, 48, -3),
+    (12, 24, 8, 256, 16, 1, 32, 48, -4),
+    (12, 16, 8, 256, 16, 1, 40, 48, -4),
+    (12, 16, 8, 256, 16, 1, 32, 52, -4),
+    (12, 16, 8, 256, 16, 9, 32, 48, -7),
+]
+
+
+@pytest.mark.parametrize("case", HEAD_BAD)
+def test_argmax_bad_arguments_rejected_before_launch(lib, case):
+    t, W, N, K, x, M, io, vo, expect = case
+    v = lambda p: ctypes.c_void_p(p or None)
+    assert lib.qlinear_argmax(t, v(W), N, K, v(x), M, v(io), v(vo), None) == expect
+
+
+EMBED_BAD = [
+    # (type, W, N, K, ids, M, out, fp16, expected)
+    (7, 16, 8, 256, 32, 1, 48, 0, -1),
+    (12, 16, 8, 300, 32, 1, 48, 0, -2),
+    (12, 16, 0, 256, 32, 1, 48, 0, -2),
+    (12, 16, 8, 256, 32, 0, 48, 1, -2),
+    (12, 0, 8, 256, 32, 1, 48, 0, -3),
+    (12, 16, 8, 256, 0, 1, 48, 0, -3),
+    (12, 16, 8, 256, 32, 1, 0, 1, -3),
+    (12, 24, 8, 256, 32, 1, 48, 0, -4),
+    (12, 16, 8, 256, 34, 1, 48, 0, -4),
+    (12, 16, 8, 256, 32, 1, 56, 1, -4),
+]
+
+
+@pytest.mark.parametrize("case", EMBED_BAD)
+def test_embed_bad_arguments_rejected_before_launch(lib, case):
+    t, W, N, K, ids, M, out, fp16, expect = case
+    v = lambda p: ctypes.c_void_p(p or None)
+    assert lib.qlinear_embed(t, v(W), N, K, v(ids), M, v(out), fp16, None) == expect

@@ -6,6 +6,8 @@ two share no code. Two independent decoders live here:
   - qlinear_oracle.c: plain C, one weight at a time, fp64, rows split over POSIX threads;
   - oracle_np.py: numpy, every field read through unpackbits.
 Both compute y[m, n] = sum_k x[m, k] * w[n, k] with w the exact dequantised weight.
+Built on them: fused.py (the SiLU-gated and RMSNorm activations and the residual add, fp64)
+and head.py (the embedding gather and the greedy output-head choice).
 """
 from __future__ import annotations
 

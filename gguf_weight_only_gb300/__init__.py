@@ -83,16 +83,24 @@ def strerror(status: int) -> str:
     return lib().qlinear_strerror(int(status)).decode()
 
 
-def _check(status: int, what: str) -> None:
+def _check(status: int, what) -> None:
     if status != 0:
+        what = what() if callable(what) else what
         extra = ""
         if status == -5:
             extra = f" (cudaError {lib().qlinear_last_cuda_error()})"
         raise QLinearError(status, f"{what}: {STATUS.get(status, status)}: {strerror(status)}{extra}")
 
 
+_block_bytes_cache: dict = {}
+
+
 def block_bytes(ggml_type: int) -> int:
-    return lib().qlinear_block_bytes(int(ggml_type))
+    t = int(ggml_type)
+    b = _block_bytes_cache.get(t)
+    if b is None:
+        b = _block_bytes_cache[t] = lib().qlinear_block_bytes(t)
+    return b
 
 
 def gemv_max_m() -> int:
@@ -120,8 +128,11 @@ def _stream_handle(stream) -> int:
 def qlinear_raw(path: str, ggml_type: int, W_ptr: int, N: int, K: int, x_ptr: int, M: int, y_ptr: int,
                 stream_handle: int) -> None:
     """Direct C-ABI call on raw device pointers (no checks beyond the library's own)."""
-    fn = {"auto": lib().qlinear, "gemv": lib().qlinear_gemv, "gemm": lib().qlinear_gemm}[path]
-    _check(fn(int(ggml_type), W_ptr, int(N), int(K), x_ptr, int(M), y_ptr, stream_handle), f"qlinear[{path}]")
+    l = lib()
+    fn = l.qlinear if path == "auto" else l.qlinear_gemv if path == "gemv" else l.qlinear_gemm if path == "gemm" else None
+    if fn is None:
+        raise ValueError(f"unknown path {path!r}")
+    _check(fn(int(ggml_type), W_ptr, int(N), int(K), x_ptr, int(M), y_ptr, stream_handle), lambda: f"qlinear[{path}]")
 
 
 def qlinear(W, ggml_type: int, N: int, K: int, x, out=None, path: str = "auto", stream=None):

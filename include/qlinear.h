@@ -27,8 +27,8 @@
  * Ownership and execution: every pointer is a device pointer owned by the caller, on the
  * current CUDA device. W and x are read-only. The call is asynchronous on `stream`
  * (a cudaStream_t; NULL = the legacy default stream): it validates, enqueues and returns
- * without synchronising. The library keeps a small per-device state (tensor-map cache,
- * kernel attributes) created on first use and never frees caller memory. Calls on
+ * without synchronising. The library keeps a small per-device state (SM count, the device
+ * status word, kernel attributes) created on first use and never frees caller memory. Calls on
  * distinct streams may run concurrently; no scratch memory is shared between calls.
  *
  * Errors: arguments are checked on the host before any launch, and a failing check

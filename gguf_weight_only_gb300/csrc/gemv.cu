@@ -28,6 +28,7 @@
 // directly yields the half pairs (b0, b2) and (b1, b3), so x is staged with each group of
 // four columns stored as [x0 x2 x1 x3] and one 8-byte read gives both B registers.
 #include <algorithm>
+#include <cstdlib>
 #include <cstdint>
 #include <cuda.h>
 
@@ -104,6 +105,7 @@ struct GemvArgs {
     uint32_t slot_bytes;     // one ring slot, rounded to 1 KB
     uint32_t red_offset, x_offset, ring_offset;
     int round_tiles;         // row tiles whose partials are reduced together (one barrier pair)
+    int m1;                  // single-token K-quant kernel (sub-blocks on the MMA's n side)
 };
 
 // Weight tensor maps, one per projection (unused entries stay zero).
@@ -416,6 +418,130 @@ __device__ __forceinline__ void superblock_iq4(uint32_t blk_a, uint32_t blk_b, c
     acc[3] += db * (d1[3] + e1[3]);
 }
 
+// ---------------------------------------------------------------- single-token K-quant path
+//
+// With one token the MMA's eight n columns would all carry the same x. Here they carry the
+// eight 32-wide sub-blocks of the superblock instead: column j of B holds x only at the
+// k-slots that come from sub-block j and zero elsewhere, so D[row][j] = sum over sub-block j
+// of q * x, unscaled. Lane (g, c) decodes qs group c of rows g, g+8 (sub-blocks 2c from the
+// low nibbles into k-slots 2c, 2c+1 and 2c+1 from the high nibbles into 2c+8, 2c+9) and holds
+// exactly D[g][2c], D[g][2c+1], D[g+8][2c], D[g+8][2c+1] afterwards: its own sub-blocks. Their
+// scales and mins are then applied once per sub-block in fp32, so the per-weight decode is only
+// a mask: the masked nibble q (or 16 q for the high nibble) read as an fp16 bit pattern is the
+// subnormal q * 2^-24 (or q * 2^-20), exact, and the tensor core multiplies subnormal fp16
+// inputs exactly (checked on GB300), so D = 2^-24 sum q x (2^-20 for the high nibbles).
+//
+// B staging (per warp, once per launch): for superblock b of the slice and sub-block j, the
+// 16 MMAs i = 2u + v (word u of the group, v = even/odd bytes) take the x pairs
+// (x[32j + 4u + v], x[32j + 4u + v + 2]). Record (b, i) holds nine 8-byte slots: slot j is
+// (b0, b1) for column j (the pair in b0 for even j, in b1 for odd j, the other half zero),
+// slot 8 is zero. Lane (g, c) reads slot g when g >> 1 == c and slot 8 otherwise, so the
+// warp's reads of one record cover 72 contiguous bytes (no bank conflicts). The fp32 sums of
+// x over every sub-block (the min term) are staged after the records.
+
+constexpr uint32_t kM1Rec = 72, kM1Sb = 16 * kM1Rec;   // record and superblock strides of the staged B
+
+// Builds the staged B records and the sub-block sums from the warp's x tile (M = 1: row
+// r = 4 b + segment of 128 bytes, chunk p of row r stored at p ^ (r & 7)).
+__device__ __forceinline__ void m1_stage(uint32_t xtile, uint32_t xexp, uint32_t xsums, int kw, int lane) {
+    const uint32_t nitems = 64u * static_cast<uint32_t>(kw);   // (superblock, sub-block, word): a multiple of 32
+    for (uint32_t q = lane; q < nitems; q += 32) {
+        const uint32_t u = q & 7u, j = (q >> 3) & 7u, b = q >> 6;
+        const uint32_t k = 32u * j + 4u * u;          // position in the superblock
+        const uint32_t r = 4u * b + (k >> 6), col = k & 63u;
+        const uint2 v = lds64(xtile + r * 128u + ((((col >> 3) ^ (r & 7u))) << 4) + ((col & 4u) << 1));
+        const uint32_t p02 = prmt(v.x, v.y, 0x5410u), p13 = prmt(v.x, v.y, 0x7632u);   // (x0, x2), (x1, x3)
+        const uint32_t e = xexp + b * kM1Sb + (2u * u) * kM1Rec + 8u * j;   // records 2u and 2u+1, slot j
+        if (j & 1u) {
+            sts64(e, 0u, p02);
+            sts64(e + kM1Rec, 0u, p13);
+        } else {
+            sts64(e, p02, 0u);
+            sts64(e + kM1Rec, p13, 0u);
+        }
+        if (j == 0u) {   // the zero slots of records 2u, 2u+1
+            sts64(e + 64u, 0u, 0u);
+            sts64(e + kM1Rec + 64u, 0u, 0u);
+        }
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
+        float sum = (f0.x + f0.y) + (f1.x + f1.y);
+        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);   // the eight words of one sub-block sit in
+        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);   // eight neighbouring lanes
+        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
+        if (u == 0u) sts32(xsums + (b * 8u + j) * 4u, __float_as_uint(sum));
+    }
+}
+
+// One superblock of rows g, g+8 for the single-token path: acc[0] (row g) and acc[1] (row
+// g+8) gain this lane's two sub-blocks. bx = the lane's slot in the superblock's first staged
+// record, sums = the superblock's eight fp32 sub-block sums of x.
+template <int TYPE>
+__device__ __forceinline__ void superblock_kq_m1(uint32_t blk_a, uint32_t blk_b, uint32_t bx, uint32_t sums, int c,
+                                                 float (&acc)[2]) {
+    constexpr bool Q5 = (TYPE == 13);
+    constexpr uint32_t QS = Q5 ? 48 : 16;
+    const uint4 ha = lds128(blk_a), hb = lds128(blk_b);
+    const uint4 qa0 = lds128(blk_a + QS + 32 * c), qa1 = lds128(blk_a + QS + 32 * c + 16);
+    const uint4 qb0 = lds128(blk_b + QS + 32 * c), qb1 = lds128(blk_b + QS + 32 * c + 16);
+    uint4 ha0 = make_uint4(0, 0, 0, 0), ha1 = ha0, hb0 = ha0, hb1 = ha0;
+    if constexpr (Q5) {
+        ha0 = lds128(blk_a + 16);
+        ha1 = lds128(blk_a + 32);
+        hb0 = lds128(blk_b + 16);
+        hb1 = lds128(blk_b + 32);
+    }
+    float d1[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint32_t rl = (4u - 2u * c) & 31u, rh = (7u - 2u * c) & 31u;   // Q5_K: bit 2c -> bit 4, 2c+1 -> bit 8
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const uint32_t wa = word_of(qa0, qa1, u), wb = word_of(qb0, qb1, u);
+        const uint32_t wa3 = wa >> 8, wb3 = wb >> 8;
+        uint32_t la02 = wa & 0x000F000Fu, la13 = wa3 & 0x000F000Fu;   // q         (bytes 0,2 / 1,3)
+        uint32_t ha02 = wa & 0x00F000F0u, ha13 = wa3 & 0x00F000F0u;   // 16 q
+        uint32_t lb02 = wb & 0x000F000Fu, lb13 = wb3 & 0x000F000Fu;
+        uint32_t hb02 = wb & 0x00F000F0u, hb13 = wb3 & 0x00F000F0u;
+        if constexpr (Q5) {
+            const uint32_t qa = word_of(ha0, ha1, u), qb = word_of(hb0, hb1, u);
+            const uint32_t qa3 = qa >> 8, qb3 = qb >> 8;
+            la02 = or_and(la02, rotl(qa, rl), 0x00100010u);
+            la13 = or_and(la13, rotl(qa3, rl), 0x00100010u);
+            ha02 = or_and(ha02, rotl(qa, rh), 0x01000100u);
+            ha13 = or_and(ha13, rotl(qa3, rh), 0x01000100u);
+            lb02 = or_and(lb02, rotl(qb, rl), 0x00100010u);
+            lb13 = or_and(lb13, rotl(qb3, rl), 0x00100010u);
+            hb02 = or_and(hb02, rotl(qb, rh), 0x01000100u);
+            hb13 = or_and(hb13, rotl(qb3, rh), 0x01000100u);
+        }
+        const uint2 B0 = lds64(bx + (2u * u) * kM1Rec), B1 = lds64(bx + (2u * u + 1u) * kM1Rec);
+        mma16816(d1, la02, lb02, ha02, hb02, B0.x, B0.y);
+        mma16816(e1, la13, lb13, ha13, hb13, B1.x, B1.y);
+    }
+    // scales and mins of sub-blocks 2c, 2c+1 (12-byte field, header words y, z, w)
+    auto scm = [&](const uint4 &h, float &s0, float &s1, float &m0, float &m1) {
+        const uint32_t A = h.y, B = h.z, C = h.w;
+        const uint32_t sc_lo4 = A & 0x3F3F3F3Fu, m_lo4 = B & 0x3F3F3F3Fu;
+        const uint32_t sc_hi4 = and_or(C, 0x0F0F0F0Fu, (A >> 2) & 0x30303030u);
+        const uint32_t m_hi4 = and_or(C >> 4, 0x0F0F0F0Fu, (B >> 2) & 0x30303030u);
+        const uint32_t sel = (2u * c) | ((2u * c + 1u) << 4);
+        const uint32_t vs = prmt(sc_lo4, sc_hi4, sel), vm = prmt(m_lo4, m_hi4, sel);
+        s0 = static_cast<float>(vs & 0xFFu);
+        s1 = static_cast<float>((vs >> 8) & 0xFFu);
+        m0 = static_cast<float>(vm & 0xFFu);
+        m1 = static_cast<float>((vm >> 8) & 0xFFu);
+    };
+    float sa0, sa1, ma0, ma1, sb0, sb1, mb0, mb1;
+    scm(ha, sa0, sa1, ma0, ma1);
+    scm(hb, sb0, sb1, mb0, mb1);
+    const uint2 xs2 = lds64(sums + 8u * c);   // sums of x over sub-blocks 2c, 2c+1
+    const float xs0 = __uint_as_float(xs2.x), xs1 = __uint_as_float(xs2.y);
+    const float da = half_lo_to_float(ha.x), dma = half_hi_to_float(ha.x);
+    const float db = half_lo_to_float(hb.x), dmb = half_hi_to_float(hb.x);
+    constexpr float k24 = 16777216.0f, k20 = 1048576.0f;   // 2^24, 2^20
+    acc[0] += da * (sa0 * k24 * (d1[0] + e1[0]) + sa1 * k20 * (d1[1] + e1[1])) - dma * (ma0 * xs0 + ma1 * xs1);
+    acc[1] += db * (sb0 * k24 * (d1[2] + e1[2]) + sb1 * k20 * (d1[3] + e1[3])) - dmb * (mb0 * xs0 + mb1 * xs1);
+}
+
 // ---------------------------------------------------------------- fused prologues
 
 // Shared-memory scratch of the RMSNorm prologue, in the free tail of the first (barrier)
@@ -499,13 +625,14 @@ constexpr int kFillGroup = 4;
 // next unit as soon as it has consumed it, across tile boundaries. The warps' 16 x 8 partial
 // tiles go to shared memory; after each round of tiles they are summed in fixed order.
 
-template <int TYPE, bool TMA, bool XRES, bool MULTI, bool PRO, bool ARGMAX>
+template <int TYPE, bool TMA, bool XRES, bool MULTI, bool PRO, bool ARGMAX, bool M1>
 __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const __grid_constant__ GemvMaps wmaps,
                                                       const __grid_constant__ CUtensorMap xmap,
                                                       const __grid_constant__ GemvArgs p) {
     constexpr int BB = GemvFmt<TYPE>::BB;
-    constexpr bool PERM = XRES && TYPE != 23;   // resident x is permuted once for the K-quant/Q6_K pairing
-    constexpr bool XSUM = XRES && (TYPE == 12 || TYPE == 13);   // staged sub-block sums of x (min term)
+    constexpr bool PERM = XRES && TYPE != 23 && !M1;   // resident x is permuted once for the K-quant/Q6_K pairing
+    constexpr bool XSUM = XRES && (TYPE == 12 || TYPE == 13) && !M1;   // staged sub-block sums of x (min term)
+    static_assert(!M1 || (XRES && (TYPE == 12 || TYPE == 13)), "single-token path: K-quants, resident x");
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
@@ -518,6 +645,8 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
     const uint32_t xbar = bar0 + 8u * D;
     const uint32_t xreg = base + p.x_offset + warp * p.x_warp_bytes;
     const uint32_t xsum_base = xreg + p.x_tx;   // XSUM: [token][superblock of the slice] x 32 bytes
+    // M1: staged B records [superblock][16 MMAs][9 slots] x 8 bytes, then fp32 sums [superblock][8]
+    const uint32_t xexp = xreg + p.x_tx, xsums = xexp + kM1Sb * p.kw;
     const uint32_t ring = base + p.ring_offset + warp * D * p.slot_bytes;
 
     const int G = gridDim.x, b = blockIdx.x;
@@ -730,6 +859,10 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
             }
             __syncwarp();
         }
+        if constexpr (M1) {   // after the tile is complete (copied, or filled by a prologue)
+            m1_stage(xreg, xexp, xsums, p.kw, lane);
+            __syncwarp();
+        }
     } else {
         pdl_wait();
         for (int s = 0; s < D && s < total; ++s) issue_next(s);
@@ -739,6 +872,7 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
     const uint32_t tok = static_cast<uint32_t>(min(g, p.M - 1));
     const uint32_t xrows = XRES ? 4u * p.kw : 4u * S;   // x rows per token in its tile
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc1[2] = {0.f, 0.f};   // M1: rows g, g+8 over this lane's sub-blocks
     int u = 0, s = 0, jt = 0;   // stage counter, ring slot, my tile counter
     uint32_t ph = 0;
     for (int round0 = 0; round0 < ntiles; round0 += p.round_tiles) {
@@ -761,15 +895,25 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
                     base_a += (static_cast<uint32_t>(ra * p.nsb + sb0) * static_cast<uint32_t>(BB)) & 15u;
                     base_b += (static_cast<uint32_t>(rb * p.nsb + sb0) * static_cast<uint32_t>(BB)) & 15u;
                 }
+                if constexpr (M1) {
+                    const uint32_t slot = ((g >> 1) == c) ? 8u * g : 64u;   // B of column g, or the zero slot
+#pragma unroll 2
+                    for (int j = 0; j < ns; ++j) {
+                        const uint32_t b = xsb0 + j;
+                        superblock_kq_m1<TYPE>(base_a + j * BB, base_b + j * BB, xexp + b * kM1Sb + slot,
+                                               xsums + 32u * b, c, acc1);
+                    }
+                } else {
 #pragma unroll 2   // two superblocks' independent decode chains can interleave
-                for (int j = 0; j < ns; ++j) {
-                    const uint32_t blk_a = base_a + j * BB, blk_b = base_b + j * BB;
-                    const uint32_t r0 = tok * xrows + 4u * (xsb0 + j);   // x row of segment 0
-                    if constexpr (TYPE == 12 || TYPE == 13)
-                        superblock_kq<TYPE, PERM, XSUM>(blk_a, blk_b, xrow(xst, r0 + c), c, acc,
-                                                        xsum_base + (tok * p.kw + xsb0 + j) * 32u);
-                    else if constexpr (TYPE == 14) superblock_q6<PERM>(blk_a, blk_b, xst, r0, c, acc);
-                    else superblock_iq4(blk_a, blk_b, xrow(xst, r0 + c), c, acc);
+                    for (int j = 0; j < ns; ++j) {
+                        const uint32_t blk_a = base_a + j * BB, blk_b = base_b + j * BB;
+                        const uint32_t r0 = tok * xrows + 4u * (xsb0 + j);   // x row of segment 0
+                        if constexpr (TYPE == 12 || TYPE == 13)
+                            superblock_kq<TYPE, PERM, XSUM>(blk_a, blk_b, xrow(xst, r0 + c), c, acc,
+                                                            xsum_base + (tok * p.kw + xsb0 + j) * 32u);
+                        else if constexpr (TYPE == 14) superblock_q6<PERM>(blk_a, blk_b, xst, r0, c, acc);
+                        else superblock_iq4(blk_a, blk_b, xrow(xst, r0 + c), c, acc);
+                    }
                 }
             }
             // Refill the slot. Its previous contents were read by this warp's ordinary loads,
@@ -785,7 +929,18 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
         // This warp's partial of tile t goes to its slot of the current round (tokens < M only);
         // warps run on without waiting for each other.
         float *pt = red + ((t - round0) * p.ks + kidx) * 16 * p.M;
-        if (2 * c < p.M) {
+        if constexpr (M1) {   // the four lanes of a row group hold its four sub-block pairs
+            float a0 = acc1[0], a1 = acc1[1];
+            a0 += __shfl_xor_sync(0xFFFFFFFFu, a0, 1);
+            a1 += __shfl_xor_sync(0xFFFFFFFFu, a1, 1);
+            a0 += __shfl_xor_sync(0xFFFFFFFFu, a0, 2);
+            a1 += __shfl_xor_sync(0xFFFFFFFFu, a1, 2);
+            if (c == 0) {
+                pt[g] = a0;
+                pt[g + 8] = a1;
+            }
+            acc1[0] = acc1[1] = 0.f;
+        } else if (2 * c < p.M) {
             pt[2 * c * 16 + g] = acc[0];
             pt[2 * c * 16 + g + 8] = acc[2];
         }
@@ -858,8 +1013,9 @@ struct GemvPlan {
 };
 
 // T: 16-row tiles over all projections. need_xres: only plans with x resident per warp (the
-// fused prologues fill that tile).
-GemvPlan make_plan(int type, int64_t T, int64_t K, int M, int num_sms, bool need_xres) {
+// fused prologues fill that tile). m1: the single-token K-quant kernel, whose resident x region
+// also holds the staged B records (1 KB per superblock), a zero block and the sub-block sums.
+GemvPlan make_plan(int type, int64_t T, int64_t K, int M, int num_sms, bool need_xres, bool m1) {
     GemvPlan pl{};
     GemvArgs &a = pl.a;
     const int bb = block_bytes_of(type);
@@ -909,7 +1065,8 @@ GemvPlan make_plan(int type, int64_t T, int64_t K, int M, int num_sms, bool need
         o.x_tx = static_cast<uint32_t>(M * (xres ? kw : S) * 512);
         o.x_bytes = xres ? 0u : o.x_tx;
         const uint32_t xsum_bytes = (type == 12 || type == 13) ? static_cast<uint32_t>(M * kw * 32) : 0u;
-        o.x_warp_bytes = xres ? ((o.x_tx + xsum_bytes + 1023u) & ~1023u) : 0u;
+        const uint32_t m1_bytes = m1 ? static_cast<uint32_t>(kw * (16 * 72) + kw * 32) : 0u;
+        o.x_warp_bytes = xres ? ((o.x_tx + (m1 ? m1_bytes : xsum_bytes) + 1023u) & ~1023u) : 0u;
         // a slot that also holds a 128-byte-swizzled x tile starts on 1 KB, weights alone on 128 B
         o.slot_bytes = xres ? ((o.w_bytes + 127u) & ~127u) : ((o.x_bytes + o.w_bytes + 1023u) & ~1023u);
         o.xres = xres ? 1 : 0;
@@ -929,7 +1086,7 @@ GemvPlan make_plan(int type, int64_t T, int64_t K, int M, int num_sms, bool need
         w = ks * tgc;
         // partials of up to round_tiles tiles (16 KB of shared memory) are reduced per round
         round_tiles = std::max(1, std::min(tmax, (16 * 1024) / (ks * 16 * M * 4)));
-        for (int xres = 1; xres >= (need_xres ? 1 : 0) && !found; --xres) {
+        for (int xres = 1; xres >= (need_xres || m1 ? 1 : 0) && !found; --xres) {
             for (int S = std::min(kw, s_max); S >= s_mult && !found; S -= s_mult) {
                 const int nst = (kw + S - 1) / S;
                 for (int D = std::min(4, std::max(2, 2 * nst)); D >= 2 && !found; --D) {
@@ -944,6 +1101,7 @@ GemvPlan make_plan(int type, int64_t T, int64_t K, int M, int num_sms, bool need
         return pl;
     }
     a.K = static_cast<int>(K);
+    a.m1 = m1 ? 1 : 0;
     a.M = M;
     a.nsb = nsb;
     a.kw = kw;
@@ -958,10 +1116,10 @@ GemvPlan make_plan(int type, int64_t T, int64_t K, int M, int num_sms, bool need
     return pl;
 }
 
-template <int TYPE, bool TMA, bool XRES, bool MULTI, bool PRO = false, bool ARGMAX = false>
+template <int TYPE, bool TMA, bool XRES, bool MULTI, bool PRO = false, bool ARGMAX = false, bool M1 = false>
 cudaError_t launch_t(const GemvMaps &wm, const CUtensorMap &xm, const GemvArgs &a, int grid, int threads,
                      size_t smem, bool pdl, cudaStream_t st) {
-    auto kern = gemv_kernel<TYPE, TMA, XRES, MULTI, PRO, ARGMAX>;
+    auto kern = gemv_kernel<TYPE, TMA, XRES, MULTI, PRO, ARGMAX, M1>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -977,6 +1135,15 @@ cudaError_t launch_t(const GemvMaps &wm, const CUtensorMap &xm, const GemvArgs &
 template <int TYPE>
 cudaError_t launch_type(bool tma, bool xres, const GemvMaps &wm, const CUtensorMap &xm, const GemvArgs &a,
                         int grid, int threads, size_t smem, bool pdl, cudaStream_t st) {
+    if constexpr (TYPE == 12 || TYPE == 13) {
+        if (a.m1) {   // single token, K-quants, x resident and rows copied by 2-D tensor copies
+            if (!xres || !tma) return cudaErrorInvalidValue;
+            if (a.best) return launch_t<TYPE, true, true, false, false, true, true>(wm, xm, a, grid, threads, smem, pdl, st);
+            if (a.pro != 0) return launch_t<TYPE, true, true, false, true, false, true>(wm, xm, a, grid, threads, smem, pdl, st);
+            if (a.nproj > 1) return launch_t<TYPE, true, true, true, false, false, true>(wm, xm, a, grid, threads, smem, pdl, st);
+            return launch_t<TYPE, true, true, false, false, false, true>(wm, xm, a, grid, threads, smem, pdl, st);
+        }
+    }
     if (a.best) {   // greedy head: one projection, x resident (the plan guarantees it)
         if (a.nproj != 1 || !xres || a.pro != 0) return cudaErrorInvalidValue;
         return tma ? launch_t<TYPE, true, true, false, false, true>(wm, xm, a, grid, threads, smem, pdl, st)
@@ -1003,6 +1170,15 @@ cudaError_t launch_type(bool tma, bool xres, const GemvMaps &wm, const CUtensorM
 
 namespace {
 
+// QL_GEMV_M1=0 selects the general kernel for single tokens as well (A/B measurement).
+bool single_token_off() {
+    static const bool off = [] {
+        const char *e = std::getenv("QL_GEMV_M1");
+        return e && e[0] == '0';
+    }();
+    return off;
+}
+
 cudaError_t launch_impl(int type, int nproj, const GemvProj *proj, const __half *x, int64_t K, int M,
                         const GemvFusion *fu, unsigned *status, int num_sms, bool pdl, cudaStream_t stream) {
     const int bb = block_bytes_of(type);
@@ -1019,7 +1195,14 @@ cudaError_t launch_impl(int type, int nproj, const GemvProj *proj, const __half 
         if (T > (int64_t(1) << 30)) return cudaErrorInvalidValue;
     }
     tile0[nproj] = static_cast<int>(T);
-    GemvPlan pl = make_plan(type, T, K, M, num_sms, pro != 0 || head);
+    // one token, K-quants: the single-token kernel when its larger x region fits (for every
+    // variant of the call, so that a prologue or the greedy head sums exactly as the plain call)
+    bool m1 = M == 1 && (type == 12 || type == 13) && !single_token_off();
+    GemvPlan pl = make_plan(type, T, K, M, num_sms, pro != 0 || head, m1);
+    if (m1 && pl.smem > 227 * 1024) {
+        m1 = false;
+        pl = make_plan(type, T, K, M, num_sms, pro != 0 || head, false);
+    }
     if (pl.smem > 227 * 1024) return cudaErrorNotSupported;
     const int64_t row_bytes = K / 256 * bb;
     for (int j = 0; j <= nproj; ++j) pl.a.tile0[j] = tile0[j];

@@ -544,11 +544,13 @@ __device__ __forceinline__ void superblock_kq_m1(uint32_t blk_a, uint32_t blk_b,
 
 // ---------------------------------------------------------------- fused prologues
 
-// Shared-memory scratch of the RMSNorm prologue, in the free tail of the first (barrier)
-// kilobyte: per-warp partial sums of h^2 for each token.
-constexpr uint32_t kSqOffset = 512;
-// ... and of the greedy-head epilogue: per-warp best keys of one token.
-constexpr uint32_t kArgOffset = 832;
+// Shared-memory scratch after the warps' ring barriers (the barrier region is padded to whole
+// kilobytes and ends at red_offset): the RMSNorm prologue's per-warp partial sums of h^2 for
+// each token, then the greedy-head epilogue's per-warp best keys of one token.
+__host__ __device__ constexpr uint32_t scratch_offset(int warps, int stages) {
+    return (8u * static_cast<uint32_t>(warps) * static_cast<uint32_t>(stages + 1) + 15u) & ~15u;
+}
+constexpr uint32_t kScratchBytes = 4u * 16u * kGemvMaxM + 8u * 16u;   // up to 16 warps
 
 // Key whose unsigned order is (value, then the smaller row): the float's bits made monotonic
 // (+0 and -0 made equal), then the row counted down from 2^32 - 1.
@@ -753,7 +755,7 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
     if constexpr (XRES) {
         for (int s = 0; s < D && s < total; ++s) issue_next(s);
         pdl_wait();
-        float *const sq = reinterpret_cast<float *>(gbase + kSqOffset);   // [warp][token]
+        float *const sq = reinterpret_cast<float *>(gbase + scratch_offset(blockDim.x >> 5, D));   // [warp][token]
         if (PRO && p.pro == 2) {
             // sum of h^2 per token: each warp a strided share of the row, fixed order
             const int kstep = static_cast<int>(blockDim.x) * 4;
@@ -956,7 +958,8 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
       if constexpr (ARGMAX) {
           // greedy head: per token, the CTA's best (value, row) key, then one atomic max;
           // each value is summed exactly as the y path sums it
-          unsigned long long *wbest = reinterpret_cast<unsigned long long *>(gbase + kArgOffset);
+          unsigned long long *wbest = reinterpret_cast<unsigned long long *>(
+              gbase + scratch_offset(blockDim.x >> 5, D) + 4u * 16u * kGemvMaxM);
           for (int m = 0; m < p.M; ++m) {
               unsigned long long bk = 0ull;
               for (int q = threadIdx.x; q < (rend - round0) * 16; q += blockDim.x) {
@@ -1070,7 +1073,7 @@ GemvPlan make_plan(int type, int64_t T, int64_t K, int M, int num_sms, bool need
         // a slot that also holds a 128-byte-swizzled x tile starts on 1 KB, weights alone on 128 B
         o.slot_bytes = xres ? ((o.w_bytes + 127u) & ~127u) : ((o.x_bytes + o.w_bytes + 1023u) & ~1023u);
         o.xres = xres ? 1 : 0;
-        const uint32_t bars = static_cast<uint32_t>((w * (D + 1) * 8 + 1023) & ~1023);
+        const uint32_t bars = (scratch_offset(w, D) + kScratchBytes + 1023u) & ~1023u;
         o.red_offset = bars;
         o.round_tiles = round_tiles;
         o.x_offset = (bars + static_cast<uint32_t>(round_tiles * ks * 16 * M * sizeof(float)) + 1023u) & ~1023u;
@@ -1096,7 +1099,7 @@ GemvPlan make_plan(int type, int64_t T, int64_t K, int M, int num_sms, bool need
             }
         }
     }
-    if (!found || w * (a.stages + 1) * 8 > static_cast<int>(kSqOffset)) {   // barriers end before the prologue scratch
+    if (!found) {
         pl.smem = SIZE_MAX;
         return pl;
     }

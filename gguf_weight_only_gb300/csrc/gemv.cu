@@ -1198,9 +1198,13 @@ cudaError_t launch_impl(int type, int nproj, const GemvProj *proj, const __half 
         if (T > (int64_t(1) << 30)) return cudaErrorInvalidValue;
     }
     tile0[nproj] = static_cast<int>(T);
-    // one token, K-quants: the single-token kernel when its larger x region fits (for every
-    // variant of the call, so that a prologue or the greedy head sums exactly as the plain call)
-    bool m1 = M == 1 && (type == 12 || type == 13) && !single_token_off();
+    // One token, K-quants: the single-token kernel when its larger x region fits and each warp
+    // has at least 8 superblocks to decode (its once-per-launch staging of x costs more than it
+    // saves on fewer: measured slower on K=4096 N=4096). The choice depends on the shape only,
+    // so a prologue or the greedy head sums exactly as the plain call does.
+    const int64_t grid = std::min<int64_t>(num_sms > 0 ? num_sms : 1, T);
+    const int64_t per_warp = (T + grid - 1) / grid * ((K / 256 + 7) / 8);   // tiles per CTA x superblocks per slice of 8
+    bool m1 = M == 1 && (type == 12 || type == 13) && per_warp >= 8 && !single_token_off();
     GemvPlan pl = make_plan(type, T, K, M, num_sms, pro != 0 || head, m1);
     if (m1 && pl.smem > 227 * 1024) {
         m1 = false;

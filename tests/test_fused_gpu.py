@@ -13,7 +13,8 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 TYPES = (12, 13, 14, 23)
-SHAPES = [(37, 1024, 1), (300, 2560, 3), (129, 768, 8), (64, 4096, 2), (16, 256, 1)]
+SHAPES = [(37, 1024, 1), (300, 2560, 3), (129, 768, 8), (64, 4096, 2), (16, 256, 1),
+          (4100, 8192, 1)]   # the last: one token on the single-token K-quant kernel
 
 
 @pytest.fixture(scope="module")

@@ -83,7 +83,8 @@ def check_choice(ql, t, W, N, K, x, idx, val):
 
 
 @pytest.mark.parametrize("t", TYPES)
-@pytest.mark.parametrize("N,K,M", [(37, 1024, 1), (1000, 2560, 3), (300, 768, 8), (16, 256, 1), (4099, 512, 2)])
+@pytest.mark.parametrize("N,K,M", [(37, 1024, 1), (1000, 2560, 3), (300, 768, 8), (16, 256, 1), (4099, 512, 2),
+                                   (4100, 8192, 1)])   # the last: the single-token K-quant kernel
 def test_argmax_matches_materialised_logits(ql, t, N, K, M):
     W = synth.weights(t, N, K, [920, t, N, K])
     x = synth.activations(M, K, [921, t, M])

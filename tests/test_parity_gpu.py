@@ -171,3 +171,16 @@ def test_full_size_sampled_rows(ql, t, K, N, M):
     ref = oracle.qlinear_rows(t, W, N, K, x, rows)
     tol = oracle.tolerance_rows(t, W, N, K, x, rows)
     check(y[:, rows], ref, tol, f"full t={t} K={K} N={N} M={M}")
+
+
+# ------------------------------------------------------------------ single-token K-quant kernel
+
+# Shapes where every warp has at least 8 superblocks, so one token takes the single-token
+# kernel (sub-blocks on the MMA's n side); every output element checked, ragged N included.
+@pytest.mark.parametrize("t", (12, 13))
+@pytest.mark.parametrize("N,K", [(4100, 8192), (2432, 16384), (8000, 4096)])
+def test_single_token_kernel_matches_oracle(ql, t, N, K):
+    W = synth.weights(t, N, K, [520, t, N, K])
+    x = synth.activations(1, K, [521, t, K])
+    y = run(ql, "auto", t, W, N, K, x)
+    check(y, oracle.qlinear(t, W, N, K, x), oracle.tolerance(t, W, N, K, x), f"single token t={t} N={N} K={K}")

@@ -21,6 +21,12 @@
 //    sub-block sums.
 //  * Per-tile partials of the warps go to shared memory; after a round of tiles they are
 //    summed over the K slices in fixed order (deterministic).
+//  * One token with K-quants (when each warp has at least 8 superblocks) takes a specialised
+//    kernel that puts the eight sub-blocks on the MMA's n side instead of tokens, feeds the
+//    quants as exact fp16 subnormals and applies scales once per sub-block in fp32 (see the
+//    single-token section below). QL_GEMV_M1=0 in the environment disables it (A/B timing).
+//  * Variants of the launch (several projections; a fused prologue; the greedy-head epilogue)
+//    are separate instantiations, so the plain kernel compiles as if they did not exist.
 // MMA fragment ownership (m16n8k16): lane = 4*g + c holds rows g and g+8 of A and k-slots
 // {2c, 2c+1, 2c+8, 2c+9}. The contraction does not care which real k sits in which slot, so
 // each lane assigns the k's it decoded to its own slots and reads x for exactly those k's.

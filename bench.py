@@ -40,7 +40,20 @@ DECODE_M = 1
 DECODE_SHAPES = synth.DECODE_8B_SHAPES                 # (K, N)
 PREFILL = (12, 4096, 12288, 512)                       # type, K, N, M
 METRIC = "qlinear weight GB/s (M=1) & TFLOP/s (M=512), % of HBM / FP16 roofline"
-BB = synth.BLOCK_BYTES
+Q6_K_A16 = 270   # Q6_K in 224-byte aligned blocks (made on the device by qlinear_repack)
+BB = {**synth.BLOCK_BYTES, Q6_K_A16: 224}
+
+
+def device_weights(t, N, K, seed, dev):
+    """Seeded weights of type t on the device; the aligned Q6_K layout is made from Q6_K
+    weights by the library's repack."""
+    import torch
+    if t != Q6_K_A16:
+        return torch.from_numpy(synth.weights(t, N, K, seed)).to(dev)
+    import gguf_weight_only_gb300 as ql
+    W = ql.repack(torch.from_numpy(synth.weights(14, N, K, seed)).to(dev), 14, N, K)
+    torch.cuda.synchronize(dev)
+    return W
 
 
 def alg_bytes(t, K, N, M):
@@ -299,7 +312,7 @@ def time_shape(t, K, N, M, path_fn, reps, dev, stream, l2, replays=3):
     import torch
     wb = N * (K // 256) * BB[t]
     Pk = max(2, int(np.ceil(2.2 * l2 / wb)))
-    W0 = torch.from_numpy(synth.weights(t, N, K, [7, t, K, N])).to(dev)
+    W0 = device_weights(t, N, K, [7, t, K, N], dev)
     Wk = [W0.clone() for _ in range(Pk)]
     x = torch.from_numpy(synth.activations(M, K, [8, t, M])).to(dev)
     y = torch.empty((M, N), dtype=torch.float32, device=dev)
@@ -392,7 +405,7 @@ def time_fused(kind, t, K, N, M, reps, dev, stream, l2, lib, replays=5):
     import torch
     wb = N * (K // 256) * BB[t]
     Pk = max(2, int(np.ceil(2.2 * l2 / wb)))
-    W0 = torch.from_numpy(synth.weights(t, N, K, [7, t, K, N])).to(dev)
+    W0 = device_weights(t, N, K, [7, t, K, N], dev)
     Wk = [W0.clone() for _ in range(Pk)]
     rng = np.random.default_rng([9, t, K, N, M])
     a = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float16 if kind == "silu" else np.float32)).to(dev)
@@ -441,7 +454,7 @@ def time_argmax(t, K, N, M, reps, dev, stream, l2, lib, replays=5):
     import torch
     wb = N * (K // 256) * BB[t]
     Pk = max(2, int(np.ceil(2.2 * l2 / wb)))
-    W0 = torch.from_numpy(synth.weights(t, N, K, [7, t, K, N])).to(dev)
+    W0 = device_weights(t, N, K, [7, t, K, N], dev)
     Wk = [W0.clone() for _ in range(Pk)]
     x = torch.from_numpy(synth.activations(M, K, [8, t, M])).to(dev)
     idx = torch.empty(M, dtype=torch.int64, device=dev)
@@ -501,8 +514,9 @@ TABLE_SHAPES = [
     (13, 5120, 17408, 1), (14, 5120, 17408, 1),
     (12, 4096, 12288, 32), (12, 4096, 12288, 128), (12, 4096, 12288, 512),
     (13, 5120, 17408, 256), (14, 5120, 17408, 256),
+    (Q6_K_A16, 5120, 17408, 1), (Q6_K_A16, 5120, 17408, 256),
 ]
-TYPE_NAMES = {12: "Q4_K", 13: "Q5_K", 14: "Q6_K", 23: "IQ4_XS"}
+TYPE_NAMES = {12: "Q4_K", 13: "Q5_K", 14: "Q6_K", 23: "IQ4_XS", Q6_K_A16: "Q6_K_A16"}
 
 
 def run_table(args):

@@ -25,7 +25,8 @@ STATUS = {0: "QL_OK", -1: "QL_ERR_TYPE", -2: "QL_ERR_SHAPE", -3: "QL_ERR_NULL", 
 EXPORTS = ("qlinear", "qlinear_gemv", "qlinear_gemm", "qlinear_block_bytes", "qlinear_gemv_max_m",
            "qlinear_strerror", "qlinear_last_cuda_error", "qlinear_device_status", "qlinear_launch_count",
            "qlinear_selftest_wait_timeout", "qlinear_multi", "qlinear_max_projections", "qlinear_silu_mul",
-           "qlinear_rmsnorm", "qlinear_argmax", "qlinear_embed")
+           "qlinear_rmsnorm", "qlinear_argmax", "qlinear_embed", "qlinear_repack")
+Q6_K_A16 = 270   # Q6_K in 224-byte aligned blocks (qlinear_repack)
 
 _lib = None
 
@@ -75,6 +76,8 @@ def lib() -> ctypes.CDLL:
         l.qlinear_argmax.restype = ctypes.c_int
         l.qlinear_embed.argtypes = [ctypes.c_int, vp, i64, i64, vp, i64, vp, ctypes.c_int, vp]
         l.qlinear_embed.restype = ctypes.c_int
+        l.qlinear_repack.argtypes = [ctypes.c_int, vp, i64, i64, vp, vp]
+        l.qlinear_repack.restype = ctypes.c_int
         _lib = l
     return _lib
 
@@ -301,6 +304,21 @@ def qlinear_embed(W, ggml_type: int, N: int, K: int, ids, fp16: bool = False, ou
         _mk(out, dt, (M, K), "out")
     _check(lib().qlinear_embed(int(ggml_type), W.data_ptr(), int(N), int(K), ids.data_ptr(), M, out.data_ptr(),
                                1 if fp16 else 0, _stream_handle(stream)), "qlinear_embed")
+    return out
+
+
+def repack(W, ggml_type: int, N: int, K: int, out=None, stream=None):
+    """Q6_K weights (uint8 CUDA tensor, 210-byte blocks) rewritten into the aligned layout
+    Q6_K_A16 (224-byte blocks); use the result with ggml_type = Q6_K_A16."""
+    import torch
+    _weights(W, ggml_type, N, K)
+    n = N * (K // 256) * 224
+    if out is None:
+        out = torch.empty(n, dtype=torch.uint8, device=W.device)
+    else:
+        _mk(out, torch.uint8, (n,), "out")
+    _check(lib().qlinear_repack(int(ggml_type), W.data_ptr(), int(N), int(K), out.data_ptr(), _stream_handle(stream)),
+           "qlinear_repack")
     return out
 
 

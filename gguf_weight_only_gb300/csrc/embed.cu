@@ -117,6 +117,7 @@ cudaError_t embed_launch(int type, const uint8_t *W, const int32_t *ids, int64_t
         case 12: e = launch<12, 144>(W, ids + m0, N, K, mc, o, half_out, status, stream); break;
         case 13: e = launch<13, 176>(W, ids + m0, N, K, mc, o, half_out, status, stream); break;
         case 14: e = launch<14, 210>(W, ids + m0, N, K, mc, o, half_out, status, stream); break;
+        case kQ6KAligned: e = launch<14, 224>(W, ids + m0, N, K, mc, o, half_out, status, stream); break;
         case 23: e = launch<23, 136>(W, ids + m0, N, K, mc, o, half_out, status, stream); break;
         default: return cudaErrorInvalidValue;
         }
@@ -126,5 +127,32 @@ cudaError_t embed_launch(int type, const uint8_t *W, const int32_t *ids, int64_t
 }
 
 int embed_launch_count(int64_t M) { return static_cast<int>((M + 65534) / 65535); }
+
+namespace {
+
+// One thread per 2-byte word of the aligned layout: words 0..104 of each 224-byte block come
+// from the 210-byte source block, words 105..111 are zero.
+__global__ void repack_q6k_kernel(const uint16_t *__restrict__ src, uint16_t *__restrict__ dst, int64_t nblocks) {
+    const int64_t total = nblocks * 112;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t b = i / 112;
+        const int w = static_cast<int>(i - b * 112);
+        dst[i] = w < 105 ? src[b * 105 + w] : static_cast<uint16_t>(0);
+    }
+}
+
+}  // namespace
+
+cudaError_t repack_q6k_aligned(const uint8_t *W_src, int64_t N, int64_t K, uint8_t *W_dst, cudaStream_t stream) {
+    const int64_t nblocks = N * (K / 256);
+    const int64_t total = nblocks * 112;
+    const int threads = 256;
+    const int64_t want = (total + threads - 1) / threads;
+    const unsigned grid = static_cast<unsigned>(want < 152 * 32 ? want : 152 * 32);
+    repack_q6k_kernel<<<grid, threads, 0, stream>>>(reinterpret_cast<const uint16_t *>(W_src),
+                                                    reinterpret_cast<uint16_t *>(W_dst), nblocks);
+    return cudaGetLastError();
+}
 
 }  // namespace ql

@@ -674,7 +674,8 @@ cudaError_t gemm_launch(int type, const uint8_t *W, const __half *x, float *y, i
     switch (type) {
     case 12: return launch_type<12>(pl.tma, xmap, wmap, a, grid, pl.smem, pdl, stream);
     case 13: return launch_type<13>(pl.tma, xmap, wmap, a, grid, pl.smem, pdl, stream);
-    case 14: return launch_type<14>(pl.tma, xmap, wmap, a, grid, pl.smem, pdl, stream);
+    case 14:
+    case kQ6KAligned: return launch_type<14>(pl.tma, xmap, wmap, a, grid, pl.smem, pdl, stream);   // bb tells them apart
     case 23: return launch_type<23>(pl.tma, xmap, wmap, a, grid, pl.smem, pdl, stream);
     default: return cudaErrorInvalidValue;
     }

@@ -63,6 +63,10 @@ struct GemvFmt<14> {   // Q6_K
     static constexpr int BB = 210, MAXW = 8;
 };
 template <>
+struct GemvFmt<kQ6KAligned> {   // Q6_K in 224-byte blocks
+    static constexpr int BB = 224, MAXW = 8;
+};
+template <>
 struct GemvFmt<23> {   // IQ4_XS
     static constexpr int BB = 136, MAXW = 8;
 };
@@ -72,6 +76,7 @@ int gemv_max_warps(int type) {
     case 12: return GemvFmt<12>::MAXW;
     case 13: return GemvFmt<13>::MAXW;
     case 14: return GemvFmt<14>::MAXW;
+    case kQ6KAligned: return GemvFmt<kQ6KAligned>::MAXW;
     default: return GemvFmt<23>::MAXW;
     }
 }
@@ -919,7 +924,8 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
                         if constexpr (TYPE == 12 || TYPE == 13)
                             superblock_kq<TYPE, PERM, XSUM>(blk_a, blk_b, xrow(xst, r0 + c), c, acc,
                                                             xsum_base + (tok * p.kw + xsb0 + j) * 32u);
-                        else if constexpr (TYPE == 14) superblock_q6<PERM>(blk_a, blk_b, xst, r0, c, acc);
+                        else if constexpr (TYPE == 14 || TYPE == kQ6KAligned)
+                            superblock_q6<PERM>(blk_a, blk_b, xst, r0, c, acc);
                         else superblock_iq4(blk_a, blk_b, xrow(xst, r0 + c), c, acc);
                     }
                 }
@@ -1260,6 +1266,8 @@ cudaError_t launch_impl(int type, int nproj, const GemvProj *proj, const __half 
     case 12: return launch_type<12>(pl.tma, pl.a.xres != 0, wm, xm, pl.a, pl.grid, threads, pl.smem, pdl, stream);
     case 13: return launch_type<13>(pl.tma, pl.a.xres != 0, wm, xm, pl.a, pl.grid, threads, pl.smem, pdl, stream);
     case 14: return launch_type<14>(pl.tma, pl.a.xres != 0, wm, xm, pl.a, pl.grid, threads, pl.smem, pdl, stream);
+    case kQ6KAligned:
+        return launch_type<kQ6KAligned>(pl.tma, pl.a.xres != 0, wm, xm, pl.a, pl.grid, threads, pl.smem, pdl, stream);
     case 23: return launch_type<23>(pl.tma, pl.a.xres != 0, wm, xm, pl.a, pl.grid, threads, pl.smem, pdl, stream);
     default: return cudaErrorInvalidValue;
     }

@@ -9,8 +9,16 @@
 namespace ql {
 
 // Bytes per 256-weight superblock of a ggml type id (Q4_K 144, Q5_K 176, Q6_K 210,
-// IQ4_XS 136), or -1.
+// IQ4_XS 136; the aligned Q6_K layout 270: 224), or -1.
 int block_bytes_of(int type);
+
+// Q6_K repacked into 224-byte blocks: each 210-byte block followed by 14 zero bytes, so every
+// block and row starts on a 16-byte boundary. Decoded exactly as Q6_K.
+constexpr int kQ6KAligned = 270;
+
+// Rewrites N x K/256 Q6_K blocks (W_src, 210 bytes each) into the aligned layout (W_dst,
+// 224 bytes each) on `stream`.
+cudaError_t repack_q6k_aligned(const uint8_t *W_src, int64_t N, int64_t K, uint8_t *W_dst, cudaStream_t stream);
 
 // ---------------------------------------------------------------- decode GEMV (gemv.cu)
 

@@ -191,6 +191,19 @@ int qlinear_multi(int type, int n_proj, const void *const *W_blocks, const int64
 
 int qlinear_max_projections(void) { return ql::kGemvMaxProj; }
 
+int qlinear_repack(int type, const void *W_src, int64_t N, int64_t K, void *W_dst, void *stream) {
+    if (type != QL_Q6_K) return QL_ERR_TYPE;
+    if (N < 1 || K < 256 || K % 256 != 0 || N > (int64_t(1) << 30) || K > (int64_t(1) << 24)) return QL_ERR_SHAPE;
+    if (!W_src || !W_dst) return QL_ERR_NULL;
+    if (misaligned(W_src) || misaligned(W_dst)) return QL_ERR_ALIGN;
+    DeviceState *s = nullptr;
+    int rc = device_state(&s);
+    if (rc != QL_OK) return rc;
+    cudaError_t e = ql::repack_q6k_aligned(static_cast<const uint8_t *>(W_src), N, K, static_cast<uint8_t *>(W_dst),
+                                           static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QL_OK : cuda_fail(e);
+}
+
 int qlinear_argmax(int type, const void *W_blocks, int64_t N, int64_t K, const void *x_fp16, int64_t M,
                    int64_t *index_out, float *value_out, void *stream) {
     int rc = validate(type, W_blocks, N, K, x_fp16, M, reinterpret_cast<const float *>(index_out));
@@ -255,7 +268,7 @@ int qlinear_gemv_max_m(void) { return ql::kGemvMaxM; }
 const char *qlinear_strerror(int status) {
     switch (status) {
     case QL_OK: return "success";
-    case QL_ERR_TYPE: return "unsupported ggml type (expected Q4_K=12, Q5_K=13, Q6_K=14, IQ4_XS=23)";
+    case QL_ERR_TYPE: return "unsupported type (expected Q4_K=12, Q5_K=13, Q6_K=14, IQ4_XS=23, aligned Q6_K=270)";
     case QL_ERR_SHAPE: return "bad shape (need K % 256 == 0, K >= 256, N >= 1, M >= 1, within 32-bit indexing)";
     case QL_ERR_NULL: return "null pointer argument";
     case QL_ERR_ALIGN: return "W, x and y must be 16-byte aligned";

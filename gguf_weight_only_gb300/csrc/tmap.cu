@@ -45,6 +45,7 @@ int block_bytes_of(int type) {
     case 12: return 144;
     case 13: return 176;
     case 14: return 210;
+    case 270: return 224;   // Q6_K in 16-byte aligned blocks (qlinear_repack)
     case 23: return 136;
     default: return -1;
     }

@@ -50,7 +50,8 @@ typedef enum {
     QL_Q4_K = 12,
     QL_Q5_K = 13,
     QL_Q6_K = 14,
-    QL_IQ4_XS = 23
+    QL_IQ4_XS = 23,
+    QL_Q6_K_A16 = 270   /* Q6_K repacked by qlinear_repack: 224-byte blocks, 16-byte aligned */
 } ql_type;
 
 typedef enum {
@@ -110,6 +111,20 @@ int qlinear_multi(int type, int n_proj, const void *const *W_blocks, const int64
 
 /* Most projections one qlinear_multi() call takes (4). */
 int qlinear_max_projections(void);
+
+/*
+ * qlinear_repack: Q6_K weights (type QL_Q6_K, 210-byte blocks) rewritten into the aligned
+ * layout QL_Q6_K_A16: every block followed by 14 zero bytes (224 bytes), so each block and
+ * each row starts on a 16-byte boundary. A 210-byte block fits a 2-D tensor copy only in stages
+ * of 8 blocks starting at multiples of 8 (the copy's inner extent and start must be 16-byte
+ * multiples), so Q6_K rows are otherwise fetched with one bulk copy per row; in the aligned
+ * layout both kernels use 2-D tensor copies. The pages leave the packed layout to the engine
+ * (test/unit/test_llm_quant_cpu.py repacks weights for its own kernels: q8_repack).
+ * Pass the result to any call with type = QL_Q6_K_A16; it decodes to the same weights.
+ * W_src: N*K/256*210 bytes; W_dst: N*K/256*224 bytes (device, 16-byte aligned, not
+ * overlapping). Asynchronous on `stream` (one kernel). type must be QL_Q6_K (else QL_ERR_TYPE).
+ */
+int qlinear_repack(int type, const void *W_src, int64_t N, int64_t K, void *W_dst, void *stream);
 
 /*
  * Decode calls with the layer's input produced inside the launch (fused prologue) and an

@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_block_bytes_and_metadata(lib):
-    assert [ql.block_bytes(t) for t in (12, 13, 14, 23)] == [144, 176, 210, 136]
+    assert [ql.block_bytes(t) for t in (12, 13, 14, 23, 270)] == [144, 176, 210, 136, 224]
     assert ql.block_bytes(2) == -1
     assert ql.gemv_max_m() == 8
     for s in range(-9, 1):
@@ -206,3 +206,23 @@ def test_embed_bad_arguments_rejected_before_launch(lib, case):
     t, W, N, K, ids, M, out, fp16, expect = case
     v = lambda p: ctypes.c_void_p(p or None)
     assert lib.qlinear_embed(t, v(W), N, K, v(ids), M, v(out), fp16, None) == expect
+
+
+REPACK_BAD = [
+    # (type, W_src, N, K, W_dst, expected)
+    (12, 16, 8, 256, 32, -1),     # only Q6_K is repacked
+    (270, 16, 8, 256, 32, -1),
+    (14, 16, 8, 300, 32, -2),
+    (14, 16, 0, 256, 32, -2),
+    (14, 0, 8, 256, 32, -3),
+    (14, 16, 8, 256, 0, -3),
+    (14, 24, 8, 256, 32, -4),
+    (14, 16, 8, 256, 40, -4),
+]
+
+
+@pytest.mark.parametrize("case", REPACK_BAD)
+def test_repack_bad_arguments_rejected_before_launch(lib, case):
+    t, src, N, K, dst, expect = case
+    v = lambda p: ctypes.c_void_p(p or None)
+    assert lib.qlinear_repack(t, v(src), N, K, v(dst), None) == expect

@@ -146,7 +146,8 @@ __device__ __forceinline__ uint4 lds128_a2(uint32_t addr) {
 }
 
 // Q6_K chunk gg: half hf = gg / 2 of the block, quarter t = 2 (gg % 2) + h, l = 0..31.
-template <int h>
+// ALIGNED: blocks start on 16-byte boundaries (the 224-byte layout).
+template <int h, bool ALIGNED = false>
 __device__ __forceinline__ void q6_chunk(uint32_t blk, int gg, uint32_t (&out)[16]) {
     const int hf = gg >> 1, t = 2 * (gg & 1) + h;
     const uint32_t d = lds16(blk + 208);
@@ -156,8 +157,9 @@ __device__ __forceinline__ void q6_chunk(uint32_t blk, int gg, uint32_t (&out)[1
     const uint32_t ds0 = hmul2(d2, hsub2(prmt(scb, 0x64646464u, 0x4040u), kH2_1152));   // l < 16
     const uint32_t ds1 = hmul2(d2, hsub2(prmt(scb, 0x64646464u, 0x4141u), kH2_1152));   // l >= 16
     const uint32_t qlo = 64 * hf + 32 * h, qho = 128 + 32 * hf;
-    const uint4 l0 = lds128_a2(blk + qlo), l1 = lds128_a2(blk + qlo + 16);
-    const uint4 g0 = lds128_a2(blk + qho), g1 = lds128_a2(blk + qho + 16);
+    auto ld16 = [](uint32_t a) { return ALIGNED ? lds128(a) : lds128_a2(a); };
+    const uint4 l0 = ld16(blk + qlo), l1 = ld16(blk + qlo + 16);
+    const uint4 g0 = ld16(blk + qho), g1 = ld16(blk + qho + 16);
     const int sh = 4 - 2 * t;   // qh bits 2t, 2t+1 -> bits 4, 5
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
@@ -217,6 +219,7 @@ __device__ __forceinline__ void dequant_superblock(uint32_t blk, const KqRow &kr
         if constexpr (TYPE == 12) kq_chunk<false, h>(blk, gg, kr, out);
         else if constexpr (TYPE == 13) kq_chunk<true, h>(blk, gg, kr, out);
         else if constexpr (TYPE == 14) q6_chunk<h>(blk, gg, out);
+        else if constexpr (TYPE == kQ6KAligned) q6_chunk<h, true>(blk, gg, out);
         else iq4_chunk<h>(blk, gg, out);
         tmem_st16(acol + 32 * gg, out);
     }
@@ -674,8 +677,8 @@ cudaError_t gemm_launch(int type, const uint8_t *W, const __half *x, float *y, i
     switch (type) {
     case 12: return launch_type<12>(pl.tma, xmap, wmap, a, grid, pl.smem, pdl, stream);
     case 13: return launch_type<13>(pl.tma, xmap, wmap, a, grid, pl.smem, pdl, stream);
-    case 14:
-    case kQ6KAligned: return launch_type<14>(pl.tma, xmap, wmap, a, grid, pl.smem, pdl, stream);   // bb tells them apart
+    case 14: return launch_type<14>(pl.tma, xmap, wmap, a, grid, pl.smem, pdl, stream);
+    case kQ6KAligned: return launch_type<kQ6KAligned>(pl.tma, xmap, wmap, a, grid, pl.smem, pdl, stream);
     case 23: return launch_type<23>(pl.tma, xmap, wmap, a, grid, pl.smem, pdl, stream);
     default: return cudaErrorInvalidValue;
     }

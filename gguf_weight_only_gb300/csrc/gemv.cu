@@ -316,7 +316,9 @@ __device__ __forceinline__ void q6_pairs(uint32_t qlw, uint32_t qhw, int t, uint
 }
 
 // xs = x tile of this stage, r0 = token row base (tok * 4S + 4j).
-template <bool PERM>
+// ALIGNED: blocks start on 16-byte boundaries (the 224-byte layout), so 16-byte loads need no
+// realignment.
+template <bool PERM, bool ALIGNED = false>
 __device__ __forceinline__ void superblock_q6(uint32_t blk_a, uint32_t blk_b, uint32_t xs, uint32_t r0, int c,
                                               float (&acc)[4]) {
     const int h = c >> 1, e = c & 1;
@@ -325,8 +327,9 @@ __device__ __forceinline__ void superblock_q6(uint32_t blk_a, uint32_t blk_b, ui
     q6_row_consts(blk_a, h, e, sca, da);
     q6_row_consts(blk_b, h, e, scb, db);
     const uint32_t offA = 64 * h + 16 * e, offB = 64 * h + 32 + 16 * e, offH = 128 + 32 * h + 16 * e;
-    const uint4 qaA = lds128_a2(blk_a + offA), qaB = lds128_a2(blk_a + offB), qaH = lds128_a2(blk_a + offH);
-    const uint4 qbA = lds128_a2(blk_b + offA), qbB = lds128_a2(blk_b + offB), qbH = lds128_a2(blk_b + offH);
+    auto ld16 = [](uint32_t a) { return ALIGNED ? lds128(a) : lds128_a2(a); };
+    const uint4 qaA = ld16(blk_a + offA), qaB = ld16(blk_a + offB), qaH = ld16(blk_a + offH);
+    const uint4 qbA = ld16(blk_b + offA), qbB = ld16(blk_b + offB), qbH = ld16(blk_b + offH);
     float d1[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
@@ -925,7 +928,7 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
                             superblock_kq<TYPE, PERM, XSUM>(blk_a, blk_b, xrow(xst, r0 + c), c, acc,
                                                             xsum_base + (tok * p.kw + xsb0 + j) * 32u);
                         else if constexpr (TYPE == 14 || TYPE == kQ6KAligned)
-                            superblock_q6<PERM>(blk_a, blk_b, xst, r0, c, acc);
+                            superblock_q6<PERM, TYPE == kQ6KAligned>(blk_a, blk_b, xst, r0, c, acc);
                         else superblock_iq4(blk_a, blk_b, xrow(xst, r0 + c), c, acc);
                     }
                 }

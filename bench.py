@@ -655,7 +655,7 @@ def run_case(args):
     build.build()
     lib = ql.lib()
     dev = torch.device("cuda", 0)
-    W = torch.from_numpy(synth.weights(t, N, K, [7, t, K, N])).to(dev)
+    W = device_weights(t, N, K, [7, t, K, N], dev)
     x = torch.from_numpy(synth.activations(M, K, [8, t, M])).to(dev)
     y = torch.empty((M, N), dtype=torch.float32, device=dev)
     sh = torch.cuda.current_stream(dev).cuda_stream

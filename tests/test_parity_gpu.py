@@ -177,8 +177,12 @@ def test_full_size_sampled_rows(ql, t, K, N, M):
 
 # Shapes where every warp has at least 8 superblocks, so one token takes the single-token
 # kernel (sub-blocks on the MMA's n side); every output element checked, ragged N included.
+# On 152 SMs the last four keep each warp's K slice (1 or 2 superblocks) in one stage and its
+# B operand in registers: slices of 2 (K=4096), of 1 (K=256), and of 2 with a last slice of 1
+# (K=1792: 2+2+2+1, K=768: 2+1).
 @pytest.mark.parametrize("t", (12, 13))
-@pytest.mark.parametrize("N,K", [(4100, 8192), (2432, 16384), (8000, 4096)])
+@pytest.mark.parametrize("N,K", [(4100, 8192), (2432, 16384), (8000, 4096), (20000, 256), (24000, 1792),
+                                 (29184, 768)])
 def test_single_token_kernel_matches_oracle(ql, t, N, K):
     W = synth.weights(t, N, K, [520, t, N, K])
     x = synth.activations(1, K, [521, t, K])

@@ -323,8 +323,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 stage = q_ring + qs * p.q_stage_bytes;
             }
             uint32_t blk = stage + r * p.row_pitch + j * p.bb;
-            if constexpr (!TMA)   // block data starts (o & 15) bytes into the row's window
-                blk += (static_cast<uint32_t>(row * p.nsb + sb - j) * static_cast<uint32_t>(p.bb)) & 15u;
+            if constexpr (!TMA)   // block data starts (o & 15) bytes into the row's window (unsigned
+                                  // arithmetic wraps modulo 2^32 and keeps the low four bits)
+                blk += ((static_cast<uint32_t>(row) * static_cast<uint32_t>(p.nsb) + static_cast<uint32_t>(sb - j)) *
+                        static_cast<uint32_t>(p.bb)) & 15u;
             KqRow kr{};
             if constexpr (TYPE == 12 || TYPE == 13) kr = kq_row(blk, h);
             ok = wait_or_abort(aempty(sa), aph ^ 1u, abort_flag, p.status);

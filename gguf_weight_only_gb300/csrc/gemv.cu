@@ -907,9 +907,11 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
                 const int ns = min(S, kb1 - sb0);
                 const uint32_t xsb0 = XRES ? static_cast<uint32_t>(si * S) : 0u;   // x superblock index base
                 uint32_t base_a = wst + g * p.row_pitch, base_b = wst + (g + 8) * p.row_pitch;
-                if constexpr (!TMA) {   // block data starts (o & 15) bytes into the row's window
-                    base_a += (static_cast<uint32_t>(ra * p.nsb + sb0) * static_cast<uint32_t>(BB)) & 15u;
-                    base_b += (static_cast<uint32_t>(rb * p.nsb + sb0) * static_cast<uint32_t>(BB)) & 15u;
+                if constexpr (!TMA) {   // block data starts (o & 15) bytes into the row's window; unsigned
+                    // arithmetic wraps modulo 2^32, which keeps the low four bits of the byte offset
+                    const uint32_t nsb = static_cast<uint32_t>(p.nsb), sbu = static_cast<uint32_t>(sb0);
+                    base_a += ((static_cast<uint32_t>(ra) * nsb + sbu) * static_cast<uint32_t>(BB)) & 15u;
+                    base_b += ((static_cast<uint32_t>(rb) * nsb + sbu) * static_cast<uint32_t>(BB)) & 15u;
                 }
                 if constexpr (M1) {
                     const uint32_t slot = ((g >> 1) == c) ? 8u * g : 64u;   // B of column g, or the zero slot

@@ -323,5 +323,7 @@ def repack(W, ggml_type: int, N: int, K: int, out=None, stream=None):
 
 
 def device_status(stream=None) -> int:
-    """Synchronise and return the device status word (0, or QL_ERR_TIMEOUT / QL_ERR_CUDA)."""
+    """Synchronise, return the device status recorded since the last call and clear it: 0, or
+    QL_ERR_TIMEOUT (a bounded wait ran out), QL_ERR_INDEX (an embedding id out of range) or
+    QL_ERR_CUDA."""
     return lib().qlinear_device_status(_stream_handle(stream))

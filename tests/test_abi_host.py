@@ -87,6 +87,27 @@ def test_python_wrapper_raises_without_cuda_tensors(lib):
         ql.qlinear(torch.zeros(144, dtype=torch.uint8), 12, 1, 256, torch.zeros(1, 256, dtype=torch.float16))
 
 
+def test_every_wrapper_rejects_host_tensors(lib):
+    """Host (CPU) tensors are refused before anything reaches the library or a device."""
+    import torch
+    W = torch.zeros(144, dtype=torch.uint8)
+    x = torch.zeros(1, 256, dtype=torch.float16)
+    f32 = torch.zeros(1, 256, dtype=torch.float32)
+    calls = [
+        lambda: ql.qlinear_multi([W, W], 12, [1, 1], 256, x),
+        lambda: ql.qlinear_silu_mul(W, 12, 1, 256, x, f32),
+        lambda: ql.qlinear_rmsnorm(W, 12, 1, 256, f32, torch.zeros(256, dtype=torch.float32), 1e-6),
+        lambda: ql.qlinear_argmax(W, 12, 1, 256, x),
+        lambda: ql.qlinear_embed(W, 12, 1, 256, torch.zeros(1, dtype=torch.int32)),
+        lambda: ql.repack(torch.zeros(210, dtype=torch.uint8), 14, 1, 256),
+    ]
+    for call in calls:
+        with pytest.raises(TypeError):
+            call()
+    with pytest.raises(ValueError):   # checked before any tensor
+        ql.qlinear_multi([W, W], 12, [1], 256, x)
+
+
 # ------------------------------------------------------------------ qlinear_multi (projections sharing x)
 
 def _multi(lib, t, W, N, K, x, M, y, n):

@@ -329,6 +329,24 @@ def test_tolerance_is_positive_and_scales():
     np.testing.assert_allclose(oracle.tolerance(23, W, 5, 512, (2 * x.astype(np.float32)).astype(np.float16)), 2 * tol)
 
 
+def test_tolerance_hand_computed():
+    """The bound is 2e-3 * sum_k |x_k w_k| per element, not 2e-3 * |sum_k x_k w_k|. Two rows:
+    row 0 has every weight 1 (d = 1, dmin = 0, sc = 1, m = 0, every nibble 1); row 1 every
+    weight 0 (d = 0). With x alternating +1, -1 over K = 256: y[0] = 0 but the bound is
+    2e-3 * 256 = 0.512; row 1 gets bound 0; doubling x doubles the bound; tolerance_rows
+    of row 0 alone equals column 0."""
+    ones = q4k_block(1.0, 0.0, [1, 1, 1, 1, 0, 0, 0, 0, 1, 1, 1, 1], 0x11)
+    zeros = q4k_block(0.0, 0.0, [1, 1, 1, 1, 0, 0, 0, 0, 1, 1, 1, 1], 0x11)
+    np.testing.assert_array_equal(dq_both(12, ones), np.ones(256))
+    W = np.concatenate([ones, zeros])
+    x = np.tile(np.array([1.0, -1.0], np.float16), 128).reshape(1, 256)
+    assert oracle.qlinear(12, W, 2, 256, x)[0, 0] == 0.0
+    tol = oracle.tolerance(12, W, 2, 256, x)
+    np.testing.assert_allclose(tol, [[0.512, 0.0]], rtol=1e-15, atol=0)
+    np.testing.assert_allclose(oracle.tolerance(12, W, 2, 256, (2 * x).astype(np.float16)), [[1.024, 0.0]], rtol=1e-15)
+    np.testing.assert_array_equal(oracle.tolerance_rows(12, W, 2, 256, x, [0]), tol[:, :1])
+
+
 def test_bad_arguments_are_rejected():
     with pytest.raises(ValueError):
         oracle.qlinear(12, np.zeros(144, np.uint8), 1, 100, np.zeros((1, 100), np.float16))

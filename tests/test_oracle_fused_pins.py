@@ -83,3 +83,22 @@ def test_fused_tolerance_widens_the_layer_bound():
     assert np.all(wide > base)
     # the extra term is 2^-10 sum|x w| + 2^-24 sum|w|: at most ~0.49 of the 2e-3 bound plus a tiny floor
     assert np.all(wide - base <= base * (2 ** -10 / 2e-3) + 2 ** -24 * np.abs(oracle.dequant(t, W, N, K)).sum(1)[None, :] + 1e-12)
+
+
+def test_fused_tolerance_hand_computed():
+    """Two Q4_K rows over K = 256: row 0 every weight 1 (d = 1, dmin = 0, sc = 1, m = 0, every
+    nibble 1), row 1 every weight 0 (d = 0); x alternating +1, -1; residual (4, -8).
+    Row 0: 2e-3 * 256 + 2^-10 * 256 + 2^-24 * 256 + 2^-23 * 4. Row 1: 2^-23 * 8 only."""
+    def block(d):
+        b = np.zeros(144, np.uint8)
+        b[0:2] = np.array([d], np.float16).view(np.uint8)
+        b[2:4] = np.array([0.0], np.float16).view(np.uint8)
+        b[4:16] = [1, 1, 1, 1, 0, 0, 0, 0, 1, 1, 1, 1]   # sc = 1, m = 0 in all eight sub-blocks
+        b[16:144] = 0x11                                  # both nibbles 1
+        return b
+    W = np.concatenate([block(1.0), block(0.0)])
+    x = np.tile(np.array([1.0, -1.0], np.float16), 128).reshape(1, 256)
+    r = np.array([[4.0, -8.0]], np.float32)
+    got = fused.tolerance_fused(12, W, 2, 256, x, r)
+    expect = [[2e-3 * 256 + 2.0 ** -10 * 256 + 2.0 ** -24 * 256 + 2.0 ** -23 * 4, 2.0 ** -23 * 8]]
+    np.testing.assert_allclose(got, expect, rtol=1e-15, atol=0)

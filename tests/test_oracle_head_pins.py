@@ -69,6 +69,22 @@ def test_argmax_ties_pick_the_first_row():
     assert idx[0] == 1 and val[0] == 256.0
 
 
+def test_argmax_nan_ranks_first_and_signed_zeros_tie():
+    # numpy's reading of argmax: a NaN ranks above every number (the first NaN wins), and
+    # -0 == +0 (the first zero wins). Row 6 as in the planted test (all weights 1, y = 256);
+    # row 2 has d = NaN, so y[2] is NaN; with x = -1 row 6 gives -256 and the zero rows tie.
+    N, K = 9, 256
+    W = np.zeros((N, 144), np.uint8)
+    W[6] = q4k_block(1.0, 0.5, [2, 2, 2, 2, 2, 2, 2, 2, 0x22, 0x22, 0x22, 0x22], 0x11)
+    W[2] = q4k_block(np.nan, 0.5, [2, 2, 2, 2, 2, 2, 2, 2, 0x22, 0x22, 0x22, 0x22], 0x11)
+    idx, val = head.argmax(12, W.reshape(-1), N, K, np.ones((1, K), np.float16))
+    assert idx[0] == 2 and np.isnan(val[0])
+    W[2] = 0
+    W[0] = q4k_block(-0.0, 0.0, [2, 2, 2, 2, 2, 2, 2, 2, 0x22, 0x22, 0x22, 0x22], 0x11)   # weights -0
+    idx, val = head.argmax(12, W.reshape(-1), N, K, -np.ones((1, K), np.float16))
+    assert idx[0] == 0 and val[0] == 0.0
+
+
 @pytest.mark.parametrize("t", (12, 13, 14, 23))
 def test_argmax_brute_force_tiny(t):
     N, K, M = 8, 512, 3

@@ -44,7 +44,8 @@ def run_multi(ql, t, Ws, Ns, K, x):
 # projections inside one CTA's run
 @pytest.mark.parametrize("t", TYPES)
 @pytest.mark.parametrize("Ns,K,M", [((37, 300, 16, 129), 1024, 1), ((7, 13), 512, 3), ((64, 1, 200), 2560, 8),
-                                    ((300, 301), 768, 2), ((129, 37, 16), 1024, 9), ((40, 24), 512, 20)])
+                                    ((300, 301), 768, 2), ((129, 37, 16), 1024, 9), ((40, 24), 512, 20),
+                                    ((200, 77), 12288, 8)])   # the last: x sent with every weight stage
 def test_multi_matches_oracle(ql, t, Ns, K, M):
     Ws = [synth.weights(t, N, K, [600, t, j, N]) for j, N in enumerate(Ns)]
     x = synth.activations(M, K, [601, t, M])

@@ -173,6 +173,20 @@ def test_full_size_sampled_rows(ql, t, K, N, M):
     check(y[:, rows], ref, tol, f"full t={t} K={K} N={N} M={M}")
 
 
+# ------------------------------------------------------------------ x per stage (decode)
+
+# Eight tokens at large K: each warp's slice of x for all tokens no longer fits in shared memory
+# beside its ring, so on 152 SMs the plan sends x with every weight stage instead (the 8B and 27B
+# down projections batched over 8 tokens, and four tokens at K=32768); every element checked.
+@pytest.mark.parametrize("t", TYPES)
+@pytest.mark.parametrize("N,K,M", [(300, 12288, 8), (300, 17408, 8), (37, 32768, 4)])
+def test_gemv_x_per_stage_matches_oracle(ql, t, N, K, M):
+    W = synth.weights(t, N, K, [540, t, N, K])
+    x = synth.activations(M, K, [541, t, M, K])
+    check(run(ql, "gemv", t, W, N, K, x), oracle.qlinear(t, W, N, K, x), oracle.tolerance(t, W, N, K, x),
+          f"gemv x per stage t={t} N={N} K={K} M={M}")
+
+
 # ------------------------------------------------------------------ single-token K-quant kernel
 
 # Shapes where every warp has at least 8 superblocks, so one token takes the single-token

@@ -40,6 +40,7 @@ DECODE_M = 1
 DECODE_SHAPES = synth.DECODE_8B_SHAPES                 # (K, N)
 PREFILL = (12, 4096, 12288, 512)                       # type, K, N, M
 METRIC = "qlinear weight GB/s (M=1) & TFLOP/s (M=512), % of HBM / FP16 roofline"
+WORKLOAD = "Q4_K decode, 8B-class layer: M=1, (K,N) in (4096,4096),(4096,1024),(4096,12288),(12288,4096)"
 Q6_K_A16 = 270   # Q6_K in 224-byte aligned blocks (made on the device by qlinear_repack)
 BB = {**synth.BLOCK_BYTES, Q6_K_A16: 224}
 
@@ -284,7 +285,7 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "fp16 x, Q4_K weights, fp32 accumulate",
         "data": "synthetic (seeded blocks and N(0,1) activations of the stated shapes)",
-        "config": {"workload": "Q4_K decode, 8B-class layer: M=1, (K,N) in (4096,4096),(4096,1024),(4096,12288),(12288,4096)",
+        "config": {"workload": WORKLOAD,
                    "weight_copies_rotated": P, "l2_bytes": l2,
                    "l2_policy": f"inputs larger than L2: {P} rotated weight copies, {P * layer_bytes / 1e6:.0f} MB",
                    "parallelism": f"replicas x{world}"},
@@ -638,7 +639,7 @@ def run_reference(args):
             "warmup": args.warmup, "ms_per_step": round(float(np.median(times)) * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": "Q4_K decode, 8B-class layer: M=1, (K,N) in (4096,4096),(4096,1024),(4096,12288),(12288,4096)",
+            "config": {"workload": WORKLOAD,
                        "parallelism": "host cores"},
             "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

@@ -283,7 +283,8 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "fp16 x, Q4_K weights, fp32 accumulate",
+        "dtype": "f16",
+        "accumulate": "f32",
         "data": "synthetic (seeded blocks and N(0,1) activations of the stated shapes)",
         "config": {"workload": WORKLOAD,
                    "weight_copies_rotated": P, "l2_bytes": l2,

@@ -173,6 +173,22 @@ def test_full_size_sampled_rows(ql, t, K, N, M):
     check(y[:, rows], ref, tol, f"full t={t} K={K} N={N} M={M}")
 
 
+# ------------------------------------------------------------------ several reduction rounds (decode)
+
+# Four tokens over N=20000 rows: on 152 SMs each CTA owns up to 9 row tiles, and its partial
+# sums for 8 tiles at a time fill the 16 KB reduction area, so it reduces in two rounds.
+@pytest.mark.parametrize("t", TYPES)
+def test_gemv_two_reduction_rounds(ql, t):
+    N, K, M = 20000, 4096, 4
+    W = synth.weights(t, N, K, [545, t])
+    x = synth.activations(M, K, [546, t])
+    y = run(ql, "gemv", t, W, N, K, x)
+    rng = np.random.default_rng(547)
+    rows = np.unique(np.concatenate([[0, 127, 128, 143, 144, N - 1], rng.choice(N, 80, replace=False)]))
+    check(y[:, rows], oracle.qlinear_rows(t, W, N, K, x, rows), oracle.tolerance_rows(t, W, N, K, x, rows),
+          f"gemv two rounds t={t}")
+
+
 # ------------------------------------------------------------------ x per stage (decode)
 
 # Eight tokens at large K: each warp's slice of x for all tokens no longer fits in shared memory

@@ -347,6 +347,18 @@ def test_tolerance_hand_computed():
     np.testing.assert_array_equal(oracle.tolerance_rows(12, W, 2, 256, x, [0]), tol[:, :1])
 
 
+@pytest.mark.parametrize("t", TYPES)
+def test_row_sampled_oracle_matches_the_dense_product(t):
+    """qlinear_rows (the sampled check at full sizes) picks row r's bytes at r * K/256 * BB:
+    unsorted and repeated rows against the independent numpy decoder's dense product."""
+    N, K, M = 11, 768, 2
+    W = synth.weights(t, N, K, [20, t])
+    x = synth.activations(M, K, [21, t])
+    rows = [10, 0, 3, 3, 7]
+    dense = x.astype(np.float64) @ oracle_np.dequant(t, W, N, K)[rows].T
+    np.testing.assert_allclose(oracle.qlinear_rows(t, W, N, K, x, rows), dense, rtol=1e-12, atol=1e-12)
+
+
 def test_bad_arguments_are_rejected():
     with pytest.raises(ValueError):
         oracle.qlinear(12, np.zeros(144, np.uint8), 1, 100, np.zeros((1, 100), np.float16))

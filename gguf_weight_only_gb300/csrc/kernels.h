@@ -38,6 +38,15 @@ struct GemvProj {
 cudaError_t gemv_launch(int type, const uint8_t *W, const __half *x, float *y, int64_t N, int64_t K, int M,
                         unsigned *status, int num_sms, bool pdl, cudaStream_t stream);
 
+// The streaming decode kernel (gemv_stream.cu): one weight matrix, M <= kGemvMaxM. Every CTA
+// owns an equal share of rows, fetched as (16-row tile, K range) units by its warps; the whole
+// share is requested before the wait for the preceding kernel when it fits in shared memory.
+// Returns cudaErrorNotSupported when x and the weight ring do not fit (gemv_launch then takes
+// the persistent kernel below).
+cudaError_t gemv_stream_launch(int type, const uint8_t *W, const __half *x, float *y, int64_t N, int64_t K, int M,
+                               unsigned *status, int num_sms, bool pdl, cudaStream_t stream);
+bool gemv_stream_supported(int type, int64_t N, int64_t K, int M, int num_sms);
+
 // y_j = x . dequant(W_j)^T for nproj <= kGemvMaxProj projections sharing x and K, in one launch:
 // the row tiles of all projections form one work list split over the persistent CTAs, and
 // each CTA's warps load their slice of x once for all of them.

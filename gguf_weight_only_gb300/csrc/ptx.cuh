@@ -15,7 +15,25 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 }
 
 // Device-side status bits (OR-ed into the word the host passes to every kernel).
-enum : uint32_t { kStatusTimeout = 1u, kStatusBadIndex = 2u };
+enum : uint32_t { kStatusTimeout = 1u, kStatusBadIndex = 2u, kStatusBounds = 4u };
+
+// Bounds checks. A QL_DEBUG build checks every shared- and global-memory range the kernels'
+// pipelines touch (copy sources and destinations, decode reads, result stores) before the
+// access; a failed check sets kStatusBounds in the status word and the access is skipped, so
+// the context stays usable and the host reads QL_ERR_BOUNDS. Ordinary builds compile the
+// checks away (in_bounds is constant true).
+#ifdef QL_DEBUG
+constexpr bool kBoundsChecks = true;
+#else
+constexpr bool kBoundsChecks = false;
+#endif
+__device__ __forceinline__ bool in_bounds(bool ok, unsigned *status) {
+    if constexpr (kBoundsChecks) {
+        if (!ok) atomicOr(status, kStatusBounds);
+        return ok;
+    }
+    return true;
+}
 
 
 // ---------------------------------------------------------------- mbarrier

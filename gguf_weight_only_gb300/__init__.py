@@ -14,12 +14,14 @@ import ctypes
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_lib", "libqlinear.so")
+# QL_DEBUG=1 in the environment loads the bounds-checking build (build.build(debug=True)).
+DEBUG = os.environ.get("QL_DEBUG", "0") not in ("", "0")
+LIB_PATH = os.path.join(_HERE, "_lib_debug" if DEBUG else "_lib", "libqlinear.so")
 
 Q4_K, Q5_K, Q6_K, IQ4_XS = 12, 13, 14, 23
 STATUS = {0: "QL_OK", -1: "QL_ERR_TYPE", -2: "QL_ERR_SHAPE", -3: "QL_ERR_NULL", -4: "QL_ERR_ALIGN",
           -5: "QL_ERR_CUDA", -6: "QL_ERR_TIMEOUT", -7: "QL_ERR_UNSUPPORTED", -8: "QL_ERR_DEVICE",
-          -9: "QL_ERR_INDEX"}
+          -9: "QL_ERR_INDEX", -10: "QL_ERR_BOUNDS"}
 # Every function include/qlinear.h declares (the symbol-export test checks this list
 # against the header).
 EXPORTS = ("qlinear", "qlinear_gemv", "qlinear_gemm", "qlinear_block_bytes", "qlinear_gemv_max_m",
@@ -128,6 +130,22 @@ def _stream_handle(stream) -> int:
     return s.cuda_stream
 
 
+def _device_of(*tensors):
+    """torch.cuda.device context of the one CUDA device all tensor arguments live on: the library
+    launches on the current device, so a call runs with its tensors' device current (and on that
+    device's current stream unless a stream is given, which must belong to it)."""
+    import torch
+    devs = {t.device for t in tensors if t is not None}
+    if len(devs) != 1:
+        raise ValueError(f"tensor arguments must all be on one CUDA device, got {sorted(map(str, devs))}")
+    return torch.cuda.device(devs.pop())
+
+
+def _check_stream(stream, tensor) -> None:
+    if stream is not None and stream.device != tensor.device:
+        raise ValueError(f"stream is on {stream.device}, the tensors on {tensor.device}")
+
+
 def qlinear_raw(path: str, ggml_type: int, W_ptr: int, N: int, K: int, x_ptr: int, M: int, y_ptr: int,
                 stream_handle: int) -> None:
     """Direct C-ABI call on raw device pointers (no checks beyond the library's own)."""
@@ -163,7 +181,9 @@ def qlinear(W, ggml_type: int, N: int, K: int, x, out=None, path: str = "auto", 
         out = torch.empty((M, N), dtype=torch.float32, device=x.device)
     elif not (out.is_cuda and out.dtype == torch.float32 and out.is_contiguous() and out.numel() >= M * N):
         raise ValueError("out must be a contiguous float32 CUDA tensor with M*N elements")
-    qlinear_raw(path, ggml_type, W.data_ptr(), N, K, x.data_ptr(), M, out.data_ptr(), _stream_handle(stream))
+    _check_stream(stream, x)
+    with _device_of(W, x, out):
+        qlinear_raw(path, ggml_type, W.data_ptr(), N, K, x.data_ptr(), M, out.data_ptr(), _stream_handle(stream))
     return out
 
 
@@ -200,8 +220,10 @@ def qlinear_multi(Ws, ggml_type: int, Ns, K: int, x, outs=None, stream=None):
     w_arr = (ctypes.c_void_p * max(n, 1))(*[W.data_ptr() for W in Ws])
     n_arr = (ctypes.c_int64 * max(n, 1))(*Ns)
     y_arr = (ctypes.c_void_p * max(n, 1))(*[o.data_ptr() for o in outs])
-    _check(lib().qlinear_multi(int(ggml_type), n, w_arr, n_arr, int(K), x.data_ptr(), M, y_arr,
-                               _stream_handle(stream)), "qlinear_multi")
+    _check_stream(stream, x)
+    with _device_of(x, *Ws, *outs):
+        _check(lib().qlinear_multi(int(ggml_type), n, w_arr, n_arr, int(K), x.data_ptr(), M, y_arr,
+                                   _stream_handle(stream)), "qlinear_multi")
     return outs
 
 
@@ -241,9 +263,11 @@ def qlinear_silu_mul(W, ggml_type: int, N: int, K: int, gate, up, residual=None,
     _mk(gate, torch.float16, (M, K), "gate")
     _mk(up, torch.float32, (M, K), "up")
     out = _fused_common(W, ggml_type, N, K, M, residual, out, gate.device)
-    _check(lib().qlinear_silu_mul(int(ggml_type), W.data_ptr(), int(N), int(K), gate.data_ptr(), up.data_ptr(), M,
-                                  residual.data_ptr() if residual is not None else None, out.data_ptr(),
-                                  _stream_handle(stream)), "qlinear_silu_mul")
+    _check_stream(stream, gate)
+    with _device_of(W, gate, up, residual, out):
+        _check(lib().qlinear_silu_mul(int(ggml_type), W.data_ptr(), int(N), int(K), gate.data_ptr(), up.data_ptr(), M,
+                                      residual.data_ptr() if residual is not None else None, out.data_ptr(),
+                                      _stream_handle(stream)), "qlinear_silu_mul")
     return out
 
 
@@ -259,10 +283,12 @@ def qlinear_rmsnorm(W, ggml_type: int, N: int, K: int, h, norm_w, eps: float, re
     if xnorm is not None:
         _mk(xnorm, torch.float16, (M, K), "xnorm")
     out = _fused_common(W, ggml_type, N, K, M, residual, out, h.device)
-    _check(lib().qlinear_rmsnorm(int(ggml_type), W.data_ptr(), int(N), int(K), h.data_ptr(), norm_w.data_ptr(),
-                                 float(eps), M, residual.data_ptr() if residual is not None else None, out.data_ptr(),
-                                 xnorm.data_ptr() if xnorm is not None else None, _stream_handle(stream)),
-           "qlinear_rmsnorm")
+    _check_stream(stream, h)
+    with _device_of(W, h, norm_w, residual, out, xnorm):
+        _check(lib().qlinear_rmsnorm(int(ggml_type), W.data_ptr(), int(N), int(K), h.data_ptr(), norm_w.data_ptr(),
+                                     float(eps), M, residual.data_ptr() if residual is not None else None,
+                                     out.data_ptr(), xnorm.data_ptr() if xnorm is not None else None,
+                                     _stream_handle(stream)), "qlinear_rmsnorm")
     return out
 
 
@@ -284,8 +310,10 @@ def qlinear_argmax(W, ggml_type: int, N: int, K: int, x, stream=None):
     _weights(W, ggml_type, N, K)
     idx = torch.empty(M, dtype=torch.int64, device=x.device)
     val = torch.empty(M, dtype=torch.float32, device=x.device)
-    _check(lib().qlinear_argmax(int(ggml_type), W.data_ptr(), int(N), int(K), x.data_ptr(), M, idx.data_ptr(),
-                                val.data_ptr(), _stream_handle(stream)), "qlinear_argmax")
+    _check_stream(stream, x)
+    with _device_of(W, x):
+        _check(lib().qlinear_argmax(int(ggml_type), W.data_ptr(), int(N), int(K), x.data_ptr(), M, idx.data_ptr(),
+                                    val.data_ptr(), _stream_handle(stream)), "qlinear_argmax")
     return idx, val
 
 
@@ -302,8 +330,10 @@ def qlinear_embed(W, ggml_type: int, N: int, K: int, ids, fp16: bool = False, ou
         out = torch.empty((M, K), dtype=dt, device=ids.device)
     else:
         _mk(out, dt, (M, K), "out")
-    _check(lib().qlinear_embed(int(ggml_type), W.data_ptr(), int(N), int(K), ids.data_ptr(), M, out.data_ptr(),
-                               1 if fp16 else 0, _stream_handle(stream)), "qlinear_embed")
+    _check_stream(stream, ids)
+    with _device_of(W, ids, out):
+        _check(lib().qlinear_embed(int(ggml_type), W.data_ptr(), int(N), int(K), ids.data_ptr(), M, out.data_ptr(),
+                                   1 if fp16 else 0, _stream_handle(stream)), "qlinear_embed")
     return out
 
 
@@ -317,13 +347,16 @@ def repack(W, ggml_type: int, N: int, K: int, out=None, stream=None):
         out = torch.empty(n, dtype=torch.uint8, device=W.device)
     else:
         _mk(out, torch.uint8, (n,), "out")
-    _check(lib().qlinear_repack(int(ggml_type), W.data_ptr(), int(N), int(K), out.data_ptr(), _stream_handle(stream)),
-           "qlinear_repack")
+    _check_stream(stream, W)
+    with _device_of(W, out):
+        _check(lib().qlinear_repack(int(ggml_type), W.data_ptr(), int(N), int(K), out.data_ptr(),
+                                    _stream_handle(stream)), "qlinear_repack")
     return out
 
 
 def device_status(stream=None) -> int:
-    """Synchronise, return the device status recorded since the last call and clear it: 0, or
+    """Take (read and clear atomically, after the stream's work) the device status recorded since
+    the last call, synchronising the stream: 0, or QL_ERR_BOUNDS (a QL_DEBUG bounds check failed),
     QL_ERR_TIMEOUT (a bounded wait ran out), QL_ERR_INDEX (an embedding id out of range) or
-    QL_ERR_CUDA."""
+    QL_ERR_CUDA. The status is one word per device, shared by all streams."""
     return lib().qlinear_device_status(_stream_handle(stream))

@@ -20,6 +20,14 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_lib")
 OBJ_DIR = os.path.join(OUT_DIR, "obj")
 LIB = os.path.join(OUT_DIR, "libqlinear.so")
+# The QL_DEBUG build: every kernel checks the shared- and global-memory ranges its pipelines
+# touch, records a failed check in the device status word (QL_ERR_BOUNDS) and skips the access.
+DEBUG_OUT_DIR = os.path.join(HERE, "_lib_debug")
+DEBUG_LIB = os.path.join(DEBUG_OUT_DIR, "libqlinear.so")
+
+
+def lib_path(debug: bool = False) -> str:
+    return DEBUG_LIB if debug else LIB
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -46,17 +54,21 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile csrc/*.cu for sm_103a and link libqlinear.so; returns the library path."""
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Compile csrc/*.cu for sm_103a and link libqlinear.so; returns the library path.
+    debug=True builds the bounds-checking QL_DEBUG library into _lib_debug/ instead."""
     deps = _deps() + [os.path.abspath(__file__)]
-    if not force and not _stale(LIB, deps):
-        return LIB
-    os.makedirs(OBJ_DIR, exist_ok=True)
+    lib, obj_dir = (DEBUG_LIB, os.path.join(DEBUG_OUT_DIR, "obj")) if debug else (LIB, OBJ_DIR)
+    if debug:
+        extra_flags = (*extra_flags, "-DQL_DEBUG")
+    if not force and not _stale(lib, deps):
+        return lib
+    os.makedirs(obj_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     cc = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(OBJ_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *_flags(extra_flags), "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -67,14 +79,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, debug="--debug" in sys.argv))

@@ -176,18 +176,23 @@ __device__ __forceinline__ void m1_superblock(uint32_t blk_a, uint32_t blk_b, ui
     float d1[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) d1[j] = ((d[0][j] + d[1][j]) + (d[2][j] + d[3][j])) + ((e[0][j] + e[1][j]) + (e[2][j] + e[3][j]));
-    // scales and mins of sub-blocks 2c, 2c+1 (12-byte field, header words y, z, w)
+    // Scales and mins of sub-blocks 2c, 2c+1 from the 12-byte field (header words y, z, w): for
+    // j < 4, sc = y.byte[j] & 63 and m = z.byte[j] & 63; for j >= 4, the low four bits come from
+    // w.byte[j-4] (low / high nibble) and the top two from y.byte[j-4] / z.byte[j-4] >> 6. Lane c
+    // needs byte pair 2c & 3 of each word: bring it to bytes 0, 1, then one shift-mask-or each.
+    // The bytes become floats through 2^23 + b (exact) minus 2^23.
+    const uint32_t pair_sel = (c & 1) ? 0x4432u : 0x4410u;
+    const bool hi = c >= 2;
+    const uint32_t sa = hi ? 2u : 0u, mA = hi ? 0x3030u : 0x3F3Fu, mC = hi ? 0x0F0Fu : 0u;
     auto scm = [&](const uint4 &h, float &s0, float &s1, float &m0, float &m1) {
-        const uint32_t A = h.y, B = h.z, Cw = h.w;
-        const uint32_t sc_lo4 = A & 0x3F3F3F3Fu, m_lo4 = B & 0x3F3F3F3Fu;
-        const uint32_t sc_hi4 = and_or(Cw, 0x0F0F0F0Fu, (A >> 2) & 0x30303030u);
-        const uint32_t m_hi4 = and_or(Cw >> 4, 0x0F0F0F0Fu, (B >> 2) & 0x30303030u);
-        const uint32_t sel = (2u * c) | ((2u * c + 1u) << 4);
-        const uint32_t vs = prmt(sc_lo4, sc_hi4, sel), vm = prmt(m_lo4, m_hi4, sel);
-        s0 = static_cast<float>(vs & 0xFFu);
-        s1 = static_cast<float>((vs >> 8) & 0xFFu);
-        m0 = static_cast<float>(vm & 0xFFu);
-        m1 = static_cast<float>((vm >> 8) & 0xFFu);
+        const uint32_t A = prmt(h.y, 0u, pair_sel), B = prmt(h.z, 0u, pair_sel), Cw = prmt(h.w, 0u, pair_sel);
+        const uint32_t sc = and_or(A >> sa, mA, Cw & mC);
+        const uint32_t mn = and_or(B >> sa, mA, (Cw >> 4) & mC);
+        constexpr float k23 = 8388608.0f;
+        s0 = __uint_as_float(prmt(sc, 0x4B000000u, 0x7440u)) - k23;
+        s1 = __uint_as_float(prmt(sc, 0x4B000000u, 0x7441u)) - k23;
+        m0 = __uint_as_float(prmt(mn, 0x4B000000u, 0x7440u)) - k23;
+        m1 = __uint_as_float(prmt(mn, 0x4B000000u, 0x7441u)) - k23;
     };
     float sa0, sa1, ma0, ma1, sb0, sb1, mb0, mb1;
     scm(ha, sa0, sa1, ma0, ma1);
@@ -479,11 +484,17 @@ __global__ void __launch_bounds__(32 * MAXW, 1) gemv_stream_kernel(const __grid_
                                             p.status);
             if (!chunk_ok) {
             } else if constexpr (M1) {
-#pragma unroll 2
-                for (int j = 0; j < ns; ++j) {
-                    const uint32_t sb = static_cast<uint32_t>(sb0 + j);
-                    m1_superblock<TYPE>(base_a + j * BB, base_b + j * BB, rec0 + sb * kM1RecSb, xs + sb * 32u, c, me, mo,
-                                        swap16, p.two24, acc1);
+                // chunks of two superblocks (all but possibly a row's last) take a straight-line
+                // body, so the compiler can interleave the two superblocks' loads and MMAs
+                const uint32_t sb = static_cast<uint32_t>(sb0), rec = rec0 + sb * kM1RecSb;
+                if (ns == 2) {
+                    m1_superblock<TYPE>(base_a, base_b, rec, xs + sb * 32u, c, me, mo, swap16, p.two24, acc1);
+                    m1_superblock<TYPE>(base_a + BB, base_b + BB, rec + kM1RecSb, xs + sb * 32u + 32u, c, me, mo, swap16,
+                                        p.two24, acc1);
+                } else {
+                    for (int j = 0; j < ns; ++j)
+                        m1_superblock<TYPE>(base_a + j * BB, base_b + j * BB, rec + j * kM1RecSb, xs + (sb + j) * 32u, c,
+                                            me, mo, swap16, p.two24, acc1);
                 }
             } else {
 #pragma unroll 2

@@ -2,6 +2,7 @@
 // state, and dispatch on M between the decode GEMV and the tcgen05 prefill GEMM.
 #include <cstdint>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "kernels.h"
@@ -10,15 +11,22 @@
 
 namespace {
 
-// Device status word: kernels OR error bits into it (a bounded wait that ran out).
+// Device status word: kernels OR error bits into it (a bounded wait that ran out, an embedding
+// id out of range, a failed bounds check of a QL_DEBUG build). qlinear_device_status takes it
+// with an atomic exchange into g_status_taken.
 __device__ unsigned g_status_word;
+__device__ unsigned g_status_taken;
 
 struct DeviceState {
     bool ready = false;
     int status = QL_OK;       // QL_OK or the error of the failed initialisation
+    int dev = 0;
     int num_sms = 0;
     bool pdl = true;          // programmatic dependent launch (QL_PDL=0 disables)
+    bool fail_launch = false; // QL_TEST_FAIL=launch: every launch reports a launch error instead
     unsigned *status_word = nullptr;
+    unsigned *status_taken = nullptr;
+    std::mutex status_mutex;  // one qlinear_device_status at a time per device
 };
 
 constexpr int kMaxDevices = 64;
@@ -49,12 +57,17 @@ int device_state(DeviceState **out) {
         if (major != 10 || minor != 3) {
             s.status = QL_ERR_DEVICE;
         } else {
-            void *p = nullptr;
+            void *p = nullptr, *q = nullptr;
             if ((e = cudaGetSymbolAddress(&p, g_status_word)) != cudaSuccess) return cuda_fail(e);
+            if ((e = cudaGetSymbolAddress(&q, g_status_taken)) != cudaSuccess) return cuda_fail(e);
             s.status_word = static_cast<unsigned *>(p);
+            s.status_taken = static_cast<unsigned *>(q);
+            s.dev = dev;
             s.num_sms = sms;
             const char *env = std::getenv("QL_PDL");
             s.pdl = !(env && env[0] == '0');
+            const char *fail = std::getenv("QL_TEST_FAIL");
+            s.fail_launch = fail && std::strcmp(fail, "launch") == 0;
             s.status = QL_OK;
         }
         s.ready = true;
@@ -63,11 +76,40 @@ int device_state(DeviceState **out) {
     return s.status;
 }
 
+// Every pointer a call hands to the kernels must be device (or managed) memory of the current
+// device: a pointer of another GPU, or plain host memory, gives QL_ERR_DEVICE before any launch.
+int check_on_device(const DeviceState &s, std::initializer_list<const void *> ptrs) {
+    for (const void *ptr : ptrs) {
+        if (!ptr) continue;
+        cudaPointerAttributes at{};
+        const cudaError_t e = cudaPointerGetAttributes(&at, ptr);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();   // an unknown pointer: not an error of the context
+            return QL_ERR_DEVICE;
+        }
+        if ((at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) || at.device != s.dev)
+            return QL_ERR_DEVICE;
+    }
+    return QL_OK;
+}
+
+// The launch-failure hook of the failure-path tests: with QL_TEST_FAIL=launch in the environment
+// (read once per device) a call that would launch returns QL_ERR_CUDA with
+// cudaErrorLaunchOutOfResources recorded, and launches nothing.
+bool launch_refused(const DeviceState &s) {
+    if (!s.fail_launch) return false;
+    t_last_cuda_error = static_cast<int>(cudaErrorLaunchOutOfResources);
+    return true;
+}
+
+// Prefill token tiles go on grid.y (at most 65535) and are at least 32 tokens: larger M is refused.
+constexpr int64_t kMaxTokens = int64_t(65535) * 32;
+
 int validate(int type, const void *W, int64_t N, int64_t K, const void *x, int64_t M, const float *y) {
     if (ql::block_bytes_of(type) < 0) return QL_ERR_TYPE;
     if (N < 1 || M < 1 || K < 256 || K % 256 != 0) return QL_ERR_SHAPE;
     // 32-bit indexing limits inside the kernels
-    if (N > (int64_t(1) << 30) || K > (int64_t(1) << 24) || M > (int64_t(1) << 24)) return QL_ERR_SHAPE;
+    if (N > (int64_t(1) << 30) || K > (int64_t(1) << 24) || M > kMaxTokens) return QL_ERR_SHAPE;
     if (M * K > (int64_t(1) << 40) || M * N > (int64_t(1) << 40)) return QL_ERR_SHAPE;
     if (!W || !x || !y) return QL_ERR_NULL;
     if ((reinterpret_cast<uintptr_t>(W) | reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u)
@@ -76,6 +118,12 @@ int validate(int type, const void *W, int64_t N, int64_t K, const void *x, int64
 }
 
 enum class Path { Auto, Gemv, Gemm };
+
+// The status word's value, cleared in the same atomic operation.
+__global__ void status_take_kernel(unsigned *word, unsigned *out) { *out = atomicExch(word, 0u); }
+
+// Does nothing: launched the ordinary way (no programmatic dependent launch) it orders the stream.
+__global__ void stream_fence_kernel() {}
 
 // One thread waits, with the library's bounded wait, on a barrier phase that never
 // completes; when the wait runs out it records the timeout in the status word.
@@ -107,6 +155,8 @@ int run(Path path, int type, const void *W, int64_t N, int64_t K, const void *x,
     if (rc != QL_OK) return rc;
     DeviceState *s = nullptr;
     if ((rc = device_state(&s)) != QL_OK) return rc;
+    if ((rc = check_on_device(*s, {W, x, y})) != QL_OK) return rc;
+    if (launch_refused(*s)) return QL_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (path == Path::Gemv || (path == Path::Auto && M <= ql::kGemvMaxM))
         return run_gemv(*s, type, W, N, K, x, M, y, st);
@@ -129,6 +179,10 @@ int run_multi(int type, int n_proj, const void *const *W, const int64_t *N, int6
     DeviceState *s = nullptr;
     int rc = device_state(&s);
     if (rc != QL_OK) return rc;
+    if ((rc = check_on_device(*s, {x})) != QL_OK) return rc;
+    for (int j = 0; j < n_proj; ++j)
+        if ((rc = check_on_device(*s, {W[j], y[j]})) != QL_OK) return rc;
+    if (launch_refused(*s)) return QL_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (M > ql::kGemvMaxM) {   // prefill: one GEMM per projection
         for (int j = 0; j < n_proj; ++j) {
@@ -159,6 +213,8 @@ int run_fused(int type, const void *W, int64_t N, int64_t K, int64_t M, const ql
     if (M > ql::kGemvMaxM) return QL_ERR_UNSUPPORTED;
     DeviceState *s = nullptr;
     if ((rc = device_state(&s)) != QL_OK) return rc;
+    if ((rc = check_on_device(*s, {W, a, b, y, f.residual, f.xnorm, f.norm_w})) != QL_OK) return rc;
+    if (launch_refused(*s)) return QL_ERR_CUDA;
     cudaError_t e = ql::gemv_launch_fused(type, static_cast<const uint8_t *>(W), y, N, K, static_cast<int>(M), f,
                                           s->status_word, s->num_sms, s->pdl, static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return QL_ERR_UNSUPPORTED;
@@ -199,8 +255,17 @@ int qlinear_repack(int type, const void *W_src, int64_t N, int64_t K, void *W_ds
     DeviceState *s = nullptr;
     int rc = device_state(&s);
     if (rc != QL_OK) return rc;
+    if ((rc = check_on_device(*s, {W_src, W_dst})) != QL_OK) return rc;
+    if (launch_refused(*s)) return QL_ERR_CUDA;
     cudaError_t e = ql::repack_q6k_aligned(static_cast<const uint8_t *>(W_src), N, K, static_cast<uint8_t *>(W_dst),
                                            static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    // The layer kernels read W before their dependency wait (programmatic dependent launch): the
+    // kernel right after the repack must not be one of them. An empty kernel launched the ordinary
+    // way starts only once the repack has completed and its writes are visible, and a layer call
+    // that follows may then start early without seeing W_dst half written.
+    stream_fence_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>();
+    e = cudaGetLastError();
     return e == cudaSuccess ? QL_OK : cuda_fail(e);
 }
 
@@ -212,6 +277,8 @@ int qlinear_argmax(int type, const void *W_blocks, int64_t N, int64_t K, const v
     if (M > ql::kGemvMaxM) return QL_ERR_UNSUPPORTED;
     DeviceState *s = nullptr;
     if ((rc = device_state(&s)) != QL_OK) return rc;
+    if ((rc = check_on_device(*s, {W_blocks, x_fp16, index_out, value_out})) != QL_OK) return rc;
+    if (launch_refused(*s)) return QL_ERR_CUDA;
     cudaError_t e = ql::gemv_launch_argmax(type, static_cast<const uint8_t *>(W_blocks), N, K,
                                            static_cast<const __half *>(x_fp16), static_cast<int>(M),
                                            reinterpret_cast<long long *>(index_out), value_out, s->status_word,
@@ -231,6 +298,8 @@ int qlinear_embed(int type, const void *W_blocks, int64_t N, int64_t K, const in
     DeviceState *s = nullptr;
     int rc = device_state(&s);
     if (rc != QL_OK) return rc;
+    if ((rc = check_on_device(*s, {W_blocks, ids, out})) != QL_OK) return rc;
+    if (launch_refused(*s)) return QL_ERR_CUDA;
     cudaError_t e = ql::embed_launch(type, static_cast<const uint8_t *>(W_blocks), ids, N, K, M, out, out_fp16 != 0,
                                      s->status_word, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? QL_OK : cuda_fail(e);
@@ -277,6 +346,7 @@ const char *qlinear_strerror(int status) {
     case QL_ERR_UNSUPPORTED: return "the requested kernel cannot run this shape";
     case QL_ERR_DEVICE: return "current device is not an sm_103 (GB300) GPU";
     case QL_ERR_INDEX: return "an index read on the device was out of range (embedding id)";
+    case QL_ERR_BOUNDS: return "a bounds check of the QL_DEBUG build failed (the access was skipped)";
     default: return "unknown status";
     }
 }
@@ -287,6 +357,7 @@ int qlinear_selftest_wait_timeout(void *stream) {
     DeviceState *s = nullptr;
     int rc = device_state(&s);
     if (rc != QL_OK) return rc;
+    if (launch_refused(*s)) return QL_ERR_CUDA;
     wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(s->status_word);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? QL_OK : cuda_fail(e);
@@ -296,11 +367,18 @@ int qlinear_device_status(void *stream) {
     DeviceState *s = nullptr;
     int rc = device_state(&s);
     if (rc != QL_OK) return rc;
-    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(s->status_mutex);
+    // read and clear in one device operation, after the stream's work: a bit another stream sets
+    // meanwhile is either taken now or kept for the next check, never lost
+    status_take_kernel<<<1, 1, 0, st>>>(s->status_word, s->status_taken);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
-    unsigned word = 0, zero = 0;
-    if ((e = cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word))) != cudaSuccess) return cuda_fail(e);
-    if (word != 0 && (e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero))) != cudaSuccess) return cuda_fail(e);
+    unsigned word = 0;
+    if ((e = cudaMemcpyAsync(&word, s->status_taken, sizeof(word), cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+        return cuda_fail(e);
+    if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e);
+    if (word & ql::kStatusBounds) return QL_ERR_BOUNDS;
     if (word & ql::kStatusTimeout) return QL_ERR_TIMEOUT;
     return word ? QL_ERR_INDEX : QL_OK;
 }

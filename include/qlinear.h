@@ -25,17 +25,28 @@
  *   y_fp32   : M x N fp32, overwritten (never accumulated into).
  *
  * Ownership and execution: every pointer is a device pointer owned by the caller, on the
- * current CUDA device. W and x are read-only. The call is asynchronous on `stream`
- * (a cudaStream_t; NULL = the legacy default stream): it validates, enqueues and returns
- * without synchronising. The library keeps a small per-device state (SM count, the device
- * status word, kernel attributes) created on first use and never frees caller memory. Calls on
- * distinct streams may run concurrently; no scratch memory is shared between calls.
+ * current CUDA device (device or managed memory of another GPU, or plain host memory, is
+ * refused with QL_ERR_DEVICE before any launch). W and x are read-only. The call is
+ * asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream): it validates,
+ * enqueues and returns without synchronising. The library keeps a small per-device state (SM
+ * count, the device status word, kernel attributes) created on first use and never frees
+ * caller memory. Calls on distinct streams may run concurrently; no scratch memory is shared
+ * between calls.
+ *
+ * Weights and the preceding kernel: the layer kernels are launched with programmatic dependent
+ * launch (unless the environment sets QL_PDL=0) and start fetching W before the kernel ahead of
+ * them in the stream has finished; only x (and the other inputs) are read after it completes.
+ * So W must not be written by the kernel that immediately precedes the call on its stream.
+ * qlinear_repack keeps this by ending with an empty ordinary launch; a caller that writes W
+ * with its own kernel right before a call puts any other work (or an event wait) in between,
+ * or sets QL_PDL=0.
  *
  * Errors: arguments are checked on the host before any launch, and a failing check
  * returns a negative ql_status with nothing enqueued. A failed launch returns
  * QL_ERR_CUDA (qlinear_last_cuda_error() gives the cudaError_t, per calling thread).
- * Device-side pipeline waits are bounded; a wait that runs out sets a device status
- * word that qlinear_device_status() reports as QL_ERR_TIMEOUT.
+ * Device-side pipeline waits are bounded; a wait that runs out sets the device's status
+ * word, which qlinear_device_status() reports as QL_ERR_TIMEOUT. The status word is one per
+ * device, shared by all streams.
  */
 #ifndef QLINEAR_H_
 #define QLINEAR_H_
@@ -57,14 +68,16 @@ typedef enum {
 typedef enum {
     QL_OK = 0,
     QL_ERR_TYPE = -1,        /* unsupported ggml type */
-    QL_ERR_SHAPE = -2,       /* K % 256 != 0, N < 1, M < 1, or a size beyond int32 indexing */
+    QL_ERR_SHAPE = -2,       /* K % 256 != 0, N < 1, M < 1, M > 65535*32, or beyond int32 indexing */
     QL_ERR_NULL = -3,        /* a required pointer is NULL */
     QL_ERR_ALIGN = -4,       /* W, x or y not 16-byte aligned */
     QL_ERR_CUDA = -5,        /* a CUDA runtime call or kernel launch failed */
     QL_ERR_TIMEOUT = -6,     /* a device-side bounded wait ran out (see qlinear_device_status) */
     QL_ERR_UNSUPPORTED = -7, /* the forced path cannot run this shape on this device */
-    QL_ERR_DEVICE = -8,      /* the current device is not an sm_103 (GB300) part */
-    QL_ERR_INDEX = -9        /* an index read on the device was out of range (see qlinear_embed) */
+    QL_ERR_DEVICE = -8,      /* the current device is not an sm_103 (GB300) part, or a pointer
+                                is not device memory of the current device */
+    QL_ERR_INDEX = -9,       /* an index read on the device was out of range (see qlinear_embed) */
+    QL_ERR_BOUNDS = -10      /* a QL_DEBUG build's bounds check failed; the access was skipped */
 } ql_status;
 
 /*
@@ -122,7 +135,9 @@ int qlinear_max_projections(void);
  * (test/unit/test_llm_quant_cpu.py repacks weights for its own kernels: q8_repack).
  * Pass the result to any call with type = QL_Q6_K_A16; it decodes to the same weights.
  * W_src: N*K/256*210 bytes; W_dst: N*K/256*224 bytes (device, 16-byte aligned, not
- * overlapping). Asynchronous on `stream` (one kernel). type must be QL_Q6_K (else QL_ERR_TYPE).
+ * overlapping). Asynchronous on `stream` (the repack kernel, then an empty ordinary launch
+ * that makes a layer call right after it safe: see "Weights and the preceding kernel").
+ * type must be QL_Q6_K (else QL_ERR_TYPE).
  */
 int qlinear_repack(int type, const void *W_src, int64_t N, int64_t K, void *W_dst, void *stream);
 
@@ -192,10 +207,12 @@ const char *qlinear_strerror(int status);
 /* cudaError_t recorded by the last QL_ERR_CUDA returned on the calling thread (0 if none). */
 int qlinear_last_cuda_error(void);
 
-/* Synchronises `stream`, then reads and clears the device status word of the current
- * device: QL_OK, QL_ERR_TIMEOUT if a bounded wait in a kernel ran out since the last
- * check, QL_ERR_INDEX if an embedding id was out of range (and no wait ran out), or
- * QL_ERR_CUDA if the synchronisation itself failed. */
+/* After the work already enqueued on `stream`, reads and clears the device status word of the
+ * current device in one atomic exchange (a one-thread kernel on `stream`), then synchronises
+ * `stream`: QL_OK; QL_ERR_BOUNDS if a QL_DEBUG build's bounds check failed; else QL_ERR_TIMEOUT
+ * if a bounded wait in a kernel ran out since the last check; else QL_ERR_INDEX if an embedding
+ * id was out of range; QL_ERR_CUDA if a CUDA call failed. The word is per device: a bit set by
+ * work on another stream is reported by whichever check takes it first, and none is lost. */
 int qlinear_device_status(void *stream);
 
 /* Number of kernels one qlinear() call of this shape launches (for launch accounting);

@@ -43,7 +43,7 @@ def test_block_bytes_and_metadata(lib):
     assert [ql.block_bytes(t) for t in (12, 13, 14, 23, 270)] == [144, 176, 210, 136, 224]
     assert ql.block_bytes(2) == -1
     assert ql.gemv_max_m() == 8
-    for s in range(-9, 1):
+    for s in range(-10, 1):
         assert isinstance(ql.strerror(s), str) and ql.strerror(s) != "unknown status"
     assert ql.strerror(-99) == "unknown status"
     assert lib.qlinear_last_cuda_error() == 0
@@ -70,6 +70,7 @@ BAD = [
     (12, 24, 8, 256, 16, 1, 16, -4),         # misaligned W
     (12, 16, 8, 256, 40, 1, 16, -4),         # misaligned x
     (12, 16, 8, 256, 16, 1, 20, -4),         # misaligned y
+    (12, 16, 8, 256, 16, 65535 * 32 + 1, 16, -2),   # more tokens than the prefill grid's token tiles
 ]
 
 

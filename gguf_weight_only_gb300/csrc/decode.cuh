@@ -103,20 +103,6 @@ struct XRow {
 __device__ __forceinline__ XRow xrow(uint32_t xst, uint32_t r) { return XRow{xst + r * 128u, (r & 7u) << 4}; }
 __device__ __forceinline__ uint4 ldx(const XRow &x, uint32_t p) { return lds128(x.base + ((p << 4) ^ x.key)); }
 
-// Accumulator chains: dependent mma.sync instructions have a long latency on this part, so each
-// decoder spreads its MMAs over four independent accumulators per operand stream and adds them at
-// the end (a fixed order: results stay deterministic).
-struct Chains {
-    float v[4][4];
-    __device__ __forceinline__ Chains() {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) v[i][j] = 0.f;
-    }
-    __device__ __forceinline__ float sum(int j) const { return (v[0][j] + v[1][j]) + (v[2][j] + v[3][j]); }
-};
-
 // ---------------------------------------------------------------- per-format superblock
 
 // Q4_K / Q5_K: lane (g, c) decodes 32-byte qs group c (sub-blocks 2c, 2c+1) of rows g, g+8.
@@ -149,8 +135,7 @@ __device__ __forceinline__ void superblock_kq(uint32_t blk_a, uint32_t blk_b, co
         hb1 = lds128(blk_b + 32 - swap16);
     }
     const KqConsts ka = kq_consts(ha, c), kb = kq_consts(hb, c);
-    Chains d1, e1;
-    float d2[4] = {0.f, 0.f, 0.f, 0.f};
+    float d1[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f}, d2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int u = 0; u < 8; u += 2) {
         const uint4 xl = ldx(xr, u >> 1);         // columns 64c + 4u .. +7   (low nibbles)
@@ -163,8 +148,8 @@ __device__ __forceinline__ void superblock_kq(uint32_t blk_a, uint32_t blk_b, co
             kq_word<Q5, PERM>(word_of(qb0, qb1, uu), word_of(hb0, hb1, uu), c, kb, lb01, lb23, hb01, hb23);
             const uint32_t x0 = v ? xl.z : xl.x, x1 = v ? xl.w : xl.y;
             const uint32_t y0 = v ? xh.z : xh.x, y1 = v ? xh.w : xh.y;
-            mma16816(d1.v[uu & 3], la01, lb01, la23, lb23, x0, x1);
-            mma16816(e1.v[uu & 3], ha01, hb01, ha23, hb23, y0, y1);
+            mma16816(d1, la01, lb01, la23, lb23, x0, x1);   // two independent accumulator chains
+            mma16816(e1, ha01, hb01, ha23, hb23, y0, y1);
             if constexpr (!XS) {
                 mma16816(d2, ka.m_lo, kb.m_lo, ka.m_lo, kb.m_lo, x0, x1);
                 mma16816(d2, ka.m_hi, kb.m_hi, ka.m_hi, kb.m_hi, y0, y1);
@@ -177,10 +162,10 @@ __device__ __forceinline__ void superblock_kq(uint32_t blk_a, uint32_t blk_b, co
     }
     const float da = half_lo_to_float(ha.x), dma = half_hi_to_float(ha.x);
     const float db = half_lo_to_float(hb.x), dmb = half_hi_to_float(hb.x);
-    acc[0] += da * (d1.sum(0) + e1.sum(0)) - dma * d2[0];
-    acc[1] += da * (d1.sum(1) + e1.sum(1)) - dma * d2[1];
-    acc[2] += db * (d1.sum(2) + e1.sum(2)) - dmb * d2[2];
-    acc[3] += db * (d1.sum(3) + e1.sum(3)) - dmb * d2[3];
+    acc[0] += da * (d1[0] + e1[0]) - dma * d2[0];
+    acc[1] += da * (d1[1] + e1[1]) - dma * d2[1];
+    acc[2] += db * (d1[2] + e1[2]) - dmb * d2[2];
+    acc[3] += db * (d1[3] + e1[3]) - dmb * d2[3];
 }
 
 // 16 bytes at a 2-byte aligned shared address, read as aligned words and realigned.
@@ -245,7 +230,7 @@ __device__ __forceinline__ void superblock_q6(uint32_t blk_a, uint32_t blk_b, ui
     auto ld16 = [](uint32_t a) { return ALIGNED ? lds128(a) : lds128_a2(a); };
     const uint4 qaA = ld16(blk_a + offA), qaB = ld16(blk_a + offB), qaH = ld16(blk_a + offH);
     const uint4 qbA = ld16(blk_b + offA), qbB = ld16(blk_b + offB), qbH = ld16(blk_b + offH);
-    Chains d1, e1;
+    float d1[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
         // columns 128h + 32t + 16e + 4u: segment 2h + t/2, chunk 4(t%2) + 2e + u/2
@@ -259,15 +244,15 @@ __device__ __forceinline__ void superblock_q6(uint32_t blk_a, uint32_t blk_b, ui
                 uint32_t a01, a23, b01, b23;
                 q6_pairs<PERM>(word4((t & 1) ? qaB : qaA, uu), word4(qaH, uu), t, sca[t], a01, a23);
                 q6_pairs<PERM>(word4((t & 1) ? qbB : qbA, uu), word4(qbH, uu), t, scb[t], b01, b23);
-                if (v) mma16816(e1.v[t], a01, b01, a23, b23, xv.z, xv.w);
-                else mma16816(d1.v[t], a01, b01, a23, b23, xv.x, xv.y);
+                if (v) mma16816(e1, a01, b01, a23, b23, xv.z, xv.w);
+                else mma16816(d1, a01, b01, a23, b23, xv.x, xv.y);
             }
         }
     }
-    acc[0] += da * (d1.sum(0) + e1.sum(0));
-    acc[1] += da * (d1.sum(1) + e1.sum(1));
-    acc[2] += db * (d1.sum(2) + e1.sum(2));
-    acc[3] += db * (d1.sum(3) + e1.sum(3));
+    acc[0] += da * (d1[0] + e1[0]);
+    acc[1] += da * (d1[1] + e1[1]);
+    acc[2] += db * (d1[2] + e1[2]);
+    acc[3] += db * (d1[3] + e1[3]);
 }
 
 // IQ4_XS codebook (test/unit/test_llm_quant_cpu.py, test_unpack_lut_dot_uop) stored as
@@ -318,7 +303,7 @@ __device__ __forceinline__ void superblock_iq4(uint32_t blk_a, uint32_t blk_b, c
     float da, db;
     iq4_row_consts(blk_a, c, lsa, nba, da);
     iq4_row_consts(blk_b, c, lsb, nbb, db);
-    Chains d1, e1;
+    float d1[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
         const uint32_t qoff = 8 + 32 * c + 16 * j;
@@ -336,15 +321,15 @@ __device__ __forceinline__ void superblock_iq4(uint32_t blk_a, uint32_t blk_b, c
                 uint32_t al01, al23, ah01, ah23, bl01, bl23, bh01, bh23;
                 iq4_word(wa, lsa[j], nba[j], al01, al23, ah01, ah23);
                 iq4_word(wb, lsb[j], nbb[j], bl01, bl23, bh01, bh23);
-                mma16816(d1.v[2 * j + (u >> 1)], al01, bl01, al23, bl23, v ? xl.z : xl.x, v ? xl.w : xl.y);
-                mma16816(e1.v[2 * j + (u >> 1)], ah01, bh01, ah23, bh23, v ? xh.z : xh.x, v ? xh.w : xh.y);
+                mma16816(d1, al01, bl01, al23, bl23, v ? xl.z : xl.x, v ? xl.w : xl.y);
+                mma16816(e1, ah01, bh01, ah23, bh23, v ? xh.z : xh.x, v ? xh.w : xh.y);
             }
         }
     }
-    acc[0] += da * (d1.sum(0) + e1.sum(0));
-    acc[1] += da * (d1.sum(1) + e1.sum(1));
-    acc[2] += db * (d1.sum(2) + e1.sum(2));
-    acc[3] += db * (d1.sum(3) + e1.sum(3));
+    acc[0] += da * (d1[0] + e1[0]);
+    acc[1] += da * (d1[1] + e1[1]);
+    acc[2] += db * (d1[2] + e1[2]);
+    acc[3] += db * (d1[3] + e1[3]);
 }
 
 }  // namespace

@@ -975,10 +975,12 @@ cudaError_t gemv_launch_multi(int type, int nproj, const GemvProj *proj, const _
 
 namespace {
 // QL_GEMV_STREAM=0 keeps single-matrix decode calls on the persistent kernel (A/B measurement).
+// The streaming kernel (gemv_stream.cu) runs plain calls only when QL_GEMV_STREAM=1: measured on
+// GB300 it is slower than this kernel on every decode shape so far.
 bool stream_kernel_off() {
     static const bool off = [] {
         const char *e = std::getenv("QL_GEMV_STREAM");
-        return e && e[0] == '0';
+        return !(e && e[0] == '1');
     }();
     return off;
 }

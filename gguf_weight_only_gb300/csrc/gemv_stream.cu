@@ -82,7 +82,6 @@ struct GsArgs {
     int xboxes;            // x tensor copies (boxes of up to 256 rows of 64 halves)
     uint32_t xbox_bytes;   // bytes one x copy delivers
     uint32_t pitch;        // bytes between rows inside a chunk buffer
-    uint32_t two24;        // 1 << 24 (a runtime operand: see shr8)
     uint32_t xb_off;       // staged x (1 KB aligned); single token: its records, then the zero block
     uint32_t xs_off;       // sums of x over 32-wide sub-blocks (K-quants)
     uint32_t red_off;      // per (tile, K range) partials when ks > 1
@@ -98,34 +97,27 @@ struct GsMaps {
 
 // ---------------------------------------------------------------- single-token K-quant superblock
 
-// Single-token x records: x permuted into the order the B fragments take it. For superblock sb,
-// sub-block (column) j and word pair p (quant words u = 2p, 2p+1 of a 32-byte group), 16 bytes
-// [X02(2p), X13(2p), X02(2p+1), X13(2p+1)] with X02(u) = (x[32j + 4u], x[32j + 4u + 2]) (the
-// nibbles of quant bytes 0 and 2 of word u: MMA d) and X13(u) = (x[32j + 4u + 1], x[32j + 4u + 3])
-// (bytes 1 and 3: MMA e). Columns are kM1RecPitch = 80 bytes (five bank groups) apart, so the
-// eight columns' chunks p fall in eight different bank groups; a column whose carrier lane reads
-// its quant halves swapped stores its pairs in that order (position p holds pair p ^ 2). Every
-// lane of row group g reads column g's record (the lanes that do not carry the column mask it
-// to zero), so a warp's record read is 8 distinct 16-byte chunks: one conflict-free wavefront.
-constexpr uint32_t kM1RecPitch = 80;                // 64 bytes of x + 16
+// Single-token x records: for superblock sb, sub-block (column) j and quant word u of a 32-byte
+// group, 16 bytes [d.b0, d.b1, e.b0, e.b1] = the B fragments the lane that carries column j feeds
+// the two MMAs of word u: X02(u) = (x[32j + 4u], x[32j + 4u + 2]) pairs with the nibbles of quant
+// bytes 0 and 2 (MMA d), X13(u) = (x[32j + 4u + 1], x[32j + 4u + 3]) with bytes 1 and 3 (MMA e);
+// an even j (low nibbles) holds them in b0 and zero in b1, an odd j the reverse. The lanes that
+// carry no column read a block of zeros, so no lane masks its B operand (the integer pipe is the
+// decode's busiest). Columns are kM1RecPitch = 144 bytes (nine bank groups) apart and a column
+// whose carrier reads its quant halves swapped stores its records in that order (position u
+// holds word u ^ 4): the eight carriers' reads of one position fall in eight different bank
+// groups (two wavefronts per warp read with the zero block).
+constexpr uint32_t kM1RecPitch = 144;               // 8 records + 16 bytes
 constexpr uint32_t kM1RecSb = 8 * kM1RecPitch;      // one superblock
-
-// x >> 8 as a multiply-high by a runtime 2^24: it runs on the FMA pipe instead of the integer
-// pipe.
-__device__ __forceinline__ uint32_t shr8(uint32_t w, uint32_t two24) {
-    uint32_t d;
-    asm("mul.hi.u32 %0, %1, %2;" : "=r"(d) : "r"(w), "r"(two24));
-    return d;
-}
+constexpr uint32_t kM1ZeroBytes = 128;              // after the last superblock
 
 // One superblock of rows g, g+8 (blk_a, blk_b) for the single-token path: acc[0] (row g) and acc[1]
-// (row g+8) gain this lane's two sub-blocks 2c, 2c+1. rec = column g's x records of this
-// superblock; me / mo = all-ones when this lane carries column g in b0 / b1 (g = 2c / 2c+1);
-// sums = the superblock's eight fp32 sub-block sums of x. swap16: see the bank-conflict note.
+// (row g+8) gain this lane's two sub-blocks 2c, 2c+1. rec = this lane's x records of this
+// superblock (column g's when the lane carries it, else the zero block); sums = the superblock's
+// eight fp32 sub-block sums of x. swap16: see the bank-conflict note.
 template <int TYPE>
 __device__ __forceinline__ void m1_superblock(uint32_t blk_a, uint32_t blk_b, uint32_t rec, uint32_t sums, int c,
-                                              uint32_t me, uint32_t mo, uint32_t swap16, uint32_t two24,
-                                              float (&acc)[2]) {
+                                              uint32_t swap16, float (&acc)[2]) {
     constexpr bool Q5 = (TYPE == 13);
     constexpr uint32_t QS = Q5 ? 48 : 16;
     const uint4 ha = lds128(blk_a), hb = lds128(blk_b);
@@ -139,28 +131,22 @@ __device__ __forceinline__ void m1_superblock(uint32_t blk_a, uint32_t blk_b, ui
         hb0 = lds128(blk_b + 16 + swap16);
         hb1 = lds128(blk_b + 32 - swap16);
     }
-    // Four independent accumulator chains per byte pair (chain u & 3): a chain of dependent
-    // mma.sync is long on this part, and short chains let a warp keep several MMAs in flight.
-    float d[4][4], e[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) d[i][j] = e[i][j] = 0.f;
+    // Two accumulator chains (bytes 0, 2 and bytes 1, 3): measured on GB300, four chains and
+    // moving the shifts to the multiply pipe were both slower.
+    float d[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
     const uint32_t rl = (4u - 2u * c) & 31u, rh = (7u - 2u * c) & 31u;   // Q5_K: bit 2c -> bit 4, 2c+1 -> bit 8
-    uint4 r = make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-        if ((u & 1) == 0) r = lds128(rec + 8u * u);   // words u, u + 1
-        const uint32_t x02 = (u & 1) ? r.z : r.x, x13 = (u & 1) ? r.w : r.y;
+        const uint4 r = lds128(rec + 16u * u);
         const uint32_t wa = word_of(qa0, qa1, u), wb = word_of(qb0, qb1, u);
-        const uint32_t wa3 = shr8(wa, two24), wb3 = shr8(wb, two24);
+        const uint32_t wa3 = wa >> 8, wb3 = wb >> 8;
         uint32_t la02 = wa & 0x000F000Fu, la13 = wa3 & 0x000F000Fu;   // q         (bytes 0,2 / 1,3)
         uint32_t ha02 = wa & 0x00F000F0u, ha13 = wa3 & 0x00F000F0u;   // 16 q
         uint32_t lb02 = wb & 0x000F000Fu, lb13 = wb3 & 0x000F000Fu;
         uint32_t hb02 = wb & 0x00F000F0u, hb13 = wb3 & 0x00F000F0u;
         if constexpr (Q5) {
             const uint32_t qa = word_of(ha0, ha1, u), qb = word_of(hb0, hb1, u);
-            const uint32_t qa3 = shr8(qa, two24), qb3 = shr8(qb, two24);
+            const uint32_t qa3 = qa >> 8, qb3 = qb >> 8;
             la02 = or_and(la02, rotl(qa, rl), 0x00100010u);
             la13 = or_and(la13, rotl(qa3, rl), 0x00100010u);
             ha02 = or_and(ha02, rotl(qa, rh), 0x01000100u);
@@ -170,12 +156,12 @@ __device__ __forceinline__ void m1_superblock(uint32_t blk_a, uint32_t blk_b, ui
             hb02 = or_and(hb02, rotl(qb, rh), 0x01000100u);
             hb13 = or_and(hb13, rotl(qb3, rh), 0x01000100u);
         }
-        mma16816(d[u & 3], la02, lb02, ha02, hb02, x02 & me, x02 & mo);
-        mma16816(e[u & 3], la13, lb13, ha13, hb13, x13 & me, x13 & mo);
+        mma16816(d, la02, lb02, ha02, hb02, r.x, r.y);
+        mma16816(e, la13, lb13, ha13, hb13, r.z, r.w);
     }
     float d1[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) d1[j] = ((d[0][j] + d[1][j]) + (d[2][j] + d[3][j])) + ((e[0][j] + e[1][j]) + (e[2][j] + e[3][j]));
+    for (int j = 0; j < 4; ++j) d1[j] = d[j] + e[j];
     // Scales and mins of sub-blocks 2c, 2c+1 from the 12-byte field (header words y, z, w): for
     // j < 4, sc = y.byte[j] & 63 and m = z.byte[j] & 63; for j >= 4, the low four bits come from
     // w.byte[j-4] (low / high nibble) and the top two from y.byte[j-4] / z.byte[j-4] >> 6. Lane c
@@ -207,38 +193,39 @@ __device__ __forceinline__ void m1_superblock(uint32_t blk_a, uint32_t blk_b, ui
 }
 
 // Single-token staging straight from global x (written by the preceding kernel, read through L2):
-// thread q builds the record chunk q = (sb, j, p) from x[8q .. 8q+7], and the four lanes of one
-// (sb, j) sum its 32 values (fp32, fixed order) into sums[sb][j]. A thread issues all of its x
-// loads before its first store, so the L2 latency is paid about once. swap: the plan's half
-// swap (columns 2, 3, 6, 7 store their pairs in swapped order).
-constexpr int kM1StageBatch = 8;   // chunks per thread per pass
+// thread q builds record q = (sb, j, u) from x[4q .. 4q+3], and the eight lanes of one (sb, j) sum
+// its 32 values (fp32, fixed order) into sums[sb][j]. A thread issues all of its x loads before
+// its first store, so the L2 latency is paid about once. swap: the plan's half swap (columns 2,
+// 3, 6, 7 store their records in swapped order). Threads 0..7 also clear the zero block.
+constexpr int kM1StageBatch = 8;   // records per thread per pass
 __device__ __forceinline__ void stage_m1(const __half *x, int nsb, uint32_t recs, uint32_t sums, int swap) {
-    const uint32_t nrec = static_cast<uint32_t>(nsb) * 32u;   // a multiple of 32: whole warps iterate together
-    const uint4 *x16 = reinterpret_cast<const uint4 *>(x);
+    const uint32_t nrec = static_cast<uint32_t>(nsb) * 64u;   // a multiple of 64: whole warps iterate together
+    const uint2 *x8 = reinterpret_cast<const uint2 *>(x);
+    if (threadIdx.x < kM1ZeroBytes / 16)
+        sts128(recs + static_cast<uint32_t>(nsb) * kM1RecSb + 16u * threadIdx.x, make_uint4(0, 0, 0, 0));
     for (uint32_t q0 = threadIdx.x; q0 < nrec; q0 += kM1StageBatch * blockDim.x) {
-        uint4 v[kM1StageBatch];
+        uint2 v[kM1StageBatch];
 #pragma unroll
         for (int i = 0; i < kM1StageBatch; ++i) {
             const uint32_t q = q0 + static_cast<uint32_t>(i) * blockDim.x;
-            v[i] = q < nrec ? __ldcg(x16 + q) : make_uint4(0u, 0u, 0u, 0u);
+            v[i] = q < nrec ? __ldcg(x8 + q) : make_uint2(0u, 0u);
         }
 #pragma unroll
         for (int i = 0; i < kM1StageBatch; ++i) {
             const uint32_t q = q0 + static_cast<uint32_t>(i) * blockDim.x;
             if (q >= nrec) break;   // uniform across the warp
-            const uint32_t sb = q >> 5, j = (q >> 2) & 7u, pp = q & 3u;
-            const uint32_t pos = pp ^ ((swap && ((j >> 1) & 1u)) ? 2u : 0u);
-            const uint4 rec = make_uint4(prmt(v[i].x, v[i].y, 0x5410u), prmt(v[i].x, v[i].y, 0x7632u),
-                                         prmt(v[i].z, v[i].w, 0x5410u), prmt(v[i].z, v[i].w, 0x7632u));
+            const uint32_t sb = q >> 6, j = (q >> 3) & 7u, u = q & 7u;
+            const uint32_t pos = u ^ ((swap && ((j >> 1) & 1u)) ? 4u : 0u);
+            const uint32_t x02 = prmt(v[i].x, v[i].y, 0x5410u), x13 = prmt(v[i].x, v[i].y, 0x7632u);
+            const uint4 rec = (j & 1u) ? make_uint4(0u, x02, 0u, x13) : make_uint4(x02, 0u, x13, 0u);
             sts128(recs + sb * kM1RecSb + j * kM1RecPitch + 16u * pos, rec);
             const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&v[i].x));
             const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&v[i].y));
-            const float2 f2 = __half22float2(*reinterpret_cast<const __half2 *>(&v[i].z));
-            const float2 f3 = __half22float2(*reinterpret_cast<const __half2 *>(&v[i].w));
-            float sum = ((f0.x + f0.y) + (f1.x + f1.y)) + ((f2.x + f2.y) + (f3.x + f3.y));
+            float sum = (f0.x + f0.y) + (f1.x + f1.y);
             sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
             sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
-            if (pp == 0) sts32(sums + (sb * 8u + j) * 4u, __float_as_uint(sum));
+            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
+            if (u == 0) sts32(sums + (sb * 8u + j) * 4u, __float_as_uint(sum));
         }
     }
 }
@@ -321,7 +308,7 @@ __global__ void __launch_bounds__(32 * MAXW, 1) gemv_stream_kernel(const __grid_
         uint32_t dyn;
         asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
         const uint32_t nsbu = static_cast<uint32_t>(p.nsb), mu = static_cast<uint32_t>(p.M);
-        const uint32_t x_need = M1 ? nsbu * kM1RecSb : static_cast<uint32_t>(p.xboxes) * p.xbox_bytes;
+        const uint32_t x_need = M1 ? nsbu * kM1RecSb + kM1ZeroBytes : static_cast<uint32_t>(p.xboxes) * p.xbox_bytes;
         const uint32_t s_need = M1 ? nsbu * 32u : (KQ ? mu * nsbu * 32u : 0u);
         const int ntile_cta = (static_cast<int>(static_cast<int64_t>(p.N) * (blockIdx.x + 1) / gridDim.x) -
                                static_cast<int>(static_cast<int64_t>(p.N) * blockIdx.x / gridDim.x) + 15) / 16;
@@ -445,9 +432,10 @@ __global__ void __launch_bounds__(32 * MAXW, 1) gemv_stream_kernel(const __grid_
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float acc1[2] = {0.f, 0.f};
     const uint32_t swap16 = (p.swap && (c & 1)) ? 16u : 0u;
-    // single token: lane (g, c) carries column g when g = 2c (in b0) or g = 2c + 1 (in b1)
-    const uint32_t me = (g == 2 * c) ? 0xFFFFFFFFu : 0u, mo = (g == 2 * c + 1) ? 0xFFFFFFFFu : 0u;
-    const uint32_t rec0 = xb + static_cast<uint32_t>(g) * kM1RecPitch;
+    // single token: lane (g, c) carries column g when g / 2 == c; the others read the zero block
+    const bool carrier = (g >> 1) == c;
+    const uint32_t rec_step = carrier ? kM1RecSb : 0u;
+    const uint32_t rec0 = carrier ? xb + static_cast<uint32_t>(g) * kM1RecPitch : xb + static_cast<uint32_t>(p.nsb) * kM1RecSb;
     const uint32_t tok = static_cast<uint32_t>(min(g, p.M - 1));
     const uint32_t xrows = static_cast<uint32_t>(p.K) / 64u;   // x rows per token
     int s = 0;
@@ -474,7 +462,7 @@ __global__ void __launch_bounds__(32 * MAXW, 1) gemv_stream_kernel(const __grid_
             if (g + 8 >= brows) base_b = base_a;
             // the chunk's blocks inside this slot; its x (records or staged rows) and sums inside theirs
             const uint32_t span = static_cast<uint32_t>(ns) * BB, sbl = static_cast<uint32_t>(sb0 + ns - 1);
-            const uint32_t x_end = M1 ? rec0 + sbl * kM1RecSb + 64u
+            const uint32_t x_end = M1 ? rec0 + sbl * rec_step + 128u
                                       : xb + (tok * xrows + 4u * sbl + 4u) * 128u;
             const uint32_t s_end = M1 ? xs + (sbl + 1u) * 32u : xs + (tok * static_cast<uint32_t>(p.nsb) + sbl + 1u) * 32u;
             const bool chunk_ok = in_bounds(ns >= 1 && sb0 + ns <= p.nsb && base_a + span <= slot + cbuf &&
@@ -486,15 +474,14 @@ __global__ void __launch_bounds__(32 * MAXW, 1) gemv_stream_kernel(const __grid_
             } else if constexpr (M1) {
                 // chunks of two superblocks (all but possibly a row's last) take a straight-line
                 // body, so the compiler can interleave the two superblocks' loads and MMAs
-                const uint32_t sb = static_cast<uint32_t>(sb0), rec = rec0 + sb * kM1RecSb;
+                const uint32_t sb = static_cast<uint32_t>(sb0), rec = rec0 + sb * rec_step;
                 if (ns == 2) {
-                    m1_superblock<TYPE>(base_a, base_b, rec, xs + sb * 32u, c, me, mo, swap16, p.two24, acc1);
-                    m1_superblock<TYPE>(base_a + BB, base_b + BB, rec + kM1RecSb, xs + sb * 32u + 32u, c, me, mo, swap16,
-                                        p.two24, acc1);
+                    m1_superblock<TYPE>(base_a, base_b, rec, xs + sb * 32u, c, swap16, acc1);
+                    m1_superblock<TYPE>(base_a + BB, base_b + BB, rec + rec_step, xs + sb * 32u + 32u, c, swap16, acc1);
                 } else {
                     for (int j = 0; j < ns; ++j)
-                        m1_superblock<TYPE>(base_a + j * BB, base_b + j * BB, rec + j * kM1RecSb, xs + (sb + j) * 32u, c,
-                                            me, mo, swap16, p.two24, acc1);
+                        m1_superblock<TYPE>(base_a + j * BB, base_b + j * BB, rec + j * rec_step, xs + (sb + j) * 32u, c,
+                                            swap16, acc1);
                 }
             } else {
 #pragma unroll 2
@@ -701,7 +688,8 @@ GsPlan gs_plan_ranges(int type, int64_t N64, int64_t K64, int M, bool m1, int G,
     }
     // staged x and its sums
     const uint32_t xbox_bytes = static_cast<uint32_t>(xbox_rows) * 128u * static_cast<uint32_t>(M);
-    const uint32_t xbytes = m1 ? static_cast<uint32_t>(nsb) * kM1RecSb : static_cast<uint32_t>(xboxes) * xbox_bytes;
+    const uint32_t xbytes = m1 ? static_cast<uint32_t>(nsb) * kM1RecSb + kM1ZeroBytes
+                               : static_cast<uint32_t>(xboxes) * xbox_bytes;
     uint32_t xsbytes = 0;
     if (m1) xsbytes = static_cast<uint32_t>(nsb) * 32u;
     else if (type == 12 || type == 13) xsbytes = static_cast<uint32_t>(M) * static_cast<uint32_t>(nsb) * 32u;
@@ -756,7 +744,6 @@ GsPlan gs_plan_ranges(int type, int64_t N64, int64_t K64, int M, bool m1, int G,
     a.xboxes = xboxes;
     a.xbox_bytes = xbox_bytes;
     a.pitch = pitch;
-    a.two24 = 1u << 24;
     a.total_bytes = N64 * row_bytes;
     pl.warps = NW;
     pl.grid = G;

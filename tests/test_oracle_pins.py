@@ -321,6 +321,36 @@ def test_packed_scale_field_is_a_bijection():
     check()
 
 
+def test_iq4_scale_field_is_a_bijection():
+    """Round trip of IQ4_XS's scale field: every assignment of eight 6-bit ls values packs into
+    scales_h (2 bytes: the high two bits of ls_j at bits 2j, 2j+1) and scales_l (4 bytes: the
+    low nibble of ls_j in nibble j) and decodes back to d (ls_j - 32) on every weight of
+    sub-block j. The field is exactly 48 bits, so every byte pattern is some assignment."""
+    hypothesis = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+
+    def pack(ls):
+        h = 0
+        low = np.zeros(4, np.uint8)
+        for j, v in enumerate(ls):
+            h |= (v >> 4) << (2 * j)
+            low[j // 2] |= (v & 15) << (4 * (j % 2))
+        return np.array([h & 0xFF, h >> 8], np.uint8), low
+
+    @hypothesis.settings(max_examples=300, deadline=None)
+    @hypothesis.given(st.lists(st.integers(0, 63), min_size=8, max_size=8), st.sampled_from([0.5, 1.0, 2.0]))
+    def check(ls, d):
+        sh, sl = pack(ls)
+        b = np.zeros(136, np.uint8)
+        b[0:2] = f16_bytes(d)
+        b[2:4] = sh
+        b[4:8] = sl
+        b[8:] = 0x88   # codebook entry 8 (= 1) in every nibble
+        np.testing.assert_array_equal(dq_both(23, b), np.repeat([d * (v - 32) for v in ls], 32))
+
+    check()
+
+
 def test_tolerance_is_positive_and_scales():
     W = synth.weights(23, 5, 512, [18])
     x = synth.activations(2, 512, [19])

@@ -45,7 +45,8 @@ def check(y, ref, tol, what):
 
 # ------------------------------------------------------------------ small / ragged shapes, both kernels
 
-GEMV_SHAPES = [(1, 256, 1), (7, 512, 3), (13, 1024, 8), (37, 768, 2), (129, 2560, 5), (300, 5120, 1), (64, 4096, 4)]
+GEMV_SHAPES = [(1, 256, 1), (7, 512, 3), (13, 1024, 8), (37, 768, 2), (129, 2560, 5), (300, 5120, 1), (64, 4096, 4),
+               (45, 1280, 7)]
 
 
 @pytest.mark.parametrize("t", TYPES)
@@ -121,6 +122,36 @@ def test_unit_activation_picks_a_column(ql, t):
     ref = w[:, ks].T
     rtol = 2 ** -11 if t in (14, 23) else 2 ** -20   # one fp16 rounding of the integer operand
     np.testing.assert_allclose(y, ref, rtol=rtol, atol=2 ** -40)
+
+
+@pytest.mark.parametrize("t", (12, 13))
+def test_unit_activation_single_token(ql, t):
+    """M = 1, x = e_k, on the single-token K-quant path: the MMA's D column of sub-block j is
+    q 2^-24 (q 2^-20 for high nibbles) exactly, the x sums are 1 or 0, and y = d sc q - dmin m
+    is formed by a few fp32 products and sums: within 2^-20 of column k of dequant(W)."""
+    N, K = 70, 768
+    W = synth.weights(t, N, K, [411, t])
+    w = oracle.dequant(t, W, N, K)
+    for k in (0, 1, 31, 32, 63, 64, 255, 256, 511, 767):
+        x = np.zeros((1, K), np.float16)
+        x[0, k] = 1.0
+        y = run(ql, "gemv", t, W, N, K, x)
+        np.testing.assert_allclose(y[0], w[:, k], rtol=2 ** -20, atol=2 ** -40, err_msg=f"t={t} k={k}")
+
+
+@pytest.mark.parametrize("t", TYPES)
+def test_unit_activation_prefill(ql, t):
+    """x = e_k through the tcgen05 prefill kernel (M = 40 tokens, token m picks column k_m):
+    its dequantisers write fp16 weights to tensor memory, one rounding to 11 significant bits."""
+    N, K = 200, 1024
+    W = synth.weights(t, N, K, [412, t])
+    w = oracle.dequant(t, W, N, K)
+    ks = [(37 * m) % K for m in range(40)]
+    x = np.zeros((len(ks), K), np.float16)
+    for m, k in enumerate(ks):
+        x[m, k] = 1.0
+    y = run(ql, "gemm", t, W, N, K, x)
+    np.testing.assert_allclose(y, w[:, ks].T, rtol=2 ** -11, atol=2 ** -40)
 
 
 @pytest.mark.parametrize("path", ["gemv", "gemm"])

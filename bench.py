@@ -188,6 +188,7 @@ def run_ours(args, rank, world, local_rank):
     ys = [torch.empty((DECODE_M, N), dtype=torch.float32, device=dev) for K, N in DECODE_SHAPES]
     stream = torch.cuda.Stream(device=dev)
     sh = stream.cuda_stream
+    stream.wait_stream(torch.cuda.current_stream(dev))   # the clones above ran on the default stream
 
     def step(i):
         Ws = copies[i % P]
@@ -210,9 +211,14 @@ def run_ours(args, rank, world, local_rank):
     with torch.cuda.graph(g, stream=stream):
         for i in range(chunk):
             step(i)
-    with torch.cuda.stream(stream):
-        g.replay()
-    torch.cuda.synchronize(dev)
+    # untimed replays for at least 50 ms, so that the timed region starts on warm clocks
+    t_warm = time.perf_counter()
+    while True:
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize(dev)
+        if time.perf_counter() - t_warm >= 0.05:
+            break
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
@@ -319,6 +325,7 @@ def time_shape(t, K, N, M, path_fn, reps, dev, stream, l2, replays=3):
     x = torch.from_numpy(synth.activations(M, K, [8, t, M])).to(dev)
     y = torch.empty((M, N), dtype=torch.float32, device=dev)
     sh = stream.cuda_stream
+    stream.wait_stream(torch.cuda.current_stream(dev))   # weight copies and inputs made on the default stream
     with torch.cuda.stream(stream):
         for i in range(3):
             path_fn(t, Wk[i % Pk].data_ptr(), N, K, x.data_ptr(), M, y.data_ptr(), sh)
@@ -358,6 +365,7 @@ def time_multi(t, K, Ns, M, reps, dev, stream, l2, lib, fused=True, replays=5):
     x = torch.from_numpy(synth.activations(M, K, [8, t, M])).to(dev)
     ys = [torch.empty((M, N), dtype=torch.float32, device=dev) for N in Ns]
     sh = stream.cuda_stream
+    stream.wait_stream(torch.cuda.current_stream(dev))   # weight copies and inputs made on the default stream
     n = len(Ns)
     n_arr = (ctypes.c_int64 * n)(*Ns)
     y_arr = (ctypes.c_void_p * n)(*[y.data_ptr() for y in ys])
@@ -414,6 +422,7 @@ def time_fused(kind, t, K, N, M, reps, dev, stream, l2, lib, replays=5):
     b = torch.from_numpy(rng.standard_normal((M, K) if kind == "silu" else (K,)).astype(np.float32)).to(dev)
     y = torch.zeros((M, N), dtype=torch.float32, device=dev)
     sh = stream.cuda_stream
+    stream.wait_stream(torch.cuda.current_stream(dev))   # weight copies and inputs made on the default stream
 
     def call(i):
         if kind == "silu":
@@ -462,6 +471,7 @@ def time_argmax(t, K, N, M, reps, dev, stream, l2, lib, replays=5):
     idx = torch.empty(M, dtype=torch.int64, device=dev)
     val = torch.empty(M, dtype=torch.float32, device=dev)
     sh = stream.cuda_stream
+    stream.wait_stream(torch.cuda.current_stream(dev))   # weight copies and inputs made on the default stream
 
     def call(i):
         rc = lib.qlinear_argmax(t, Wk[i % Pk].data_ptr(), N, K, x.data_ptr(), M, idx.data_ptr(), val.data_ptr(), sh)

@@ -64,10 +64,20 @@ struct GemmArgs {
 
 // ------------------------------------------------------------ per-row dequantisers
 // Each produces the 32 fp16 weights k = 32h .. 32h+31 of 64-wide chunk gg of one row as 16
-// packed pairs (k, k+1), i.e. the 16 TMEM columns [16h, 16h+16) of that chunk.
+// packed pairs (k, k+1), i.e. the 16 TMEM columns [16h, 16h+16) of that chunk. Every weight is
+// formed in fp32 from exact parts (the integer code as an exact fp16 pair, the scale products
+// d*sc and dmin*m exact in fp32) and rounded to fp16 once: the MMA operand is the weight to
+// within one fp16 rounding, also where d*sc*q and dmin*m nearly cancel.
+
+// (q0, q1) exact integers in fp16 -> fp16x2(q0 * s + o, q1 * s + o), each rounded once
+__device__ __forceinline__ uint32_t scale_pair(uint32_t q2, float s, float o) {
+    const float2 q = __half22float2(*reinterpret_cast<const __half2 *>(&q2));
+    const __half2 r = __floats2half2_rn(fmaf(q.x, s, o), fmaf(q.y, s, o));
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
 
 struct KqRow {
-    uint32_t ds[4], ndm[4];   // (d*sc, .), (-dmin*m, .) of sub-blocks 2gg + h, gg = 0..3
+    float ds[4], ndm[4];   // d*sc and -dmin*m of sub-blocks 2gg + h, gg = 0..3 (exact in fp32)
 };
 
 __device__ __forceinline__ KqRow kq_row(uint32_t blk, int h) {
@@ -79,15 +89,12 @@ __device__ __forceinline__ KqRow kq_row(uint32_t blk, int h) {
     // pool byte j = value of sub-block j; pick j = h, 2+h, 4+h, 6+h
     const uint32_t sel = static_cast<uint32_t>(h) | ((2u + h) << 4) | ((4u + h) << 8) | ((6u + h) << 12);
     const uint32_t sc4 = prmt(sc_lo4, sc_hi4, sel), m4 = prmt(m_lo4, m_hi4, sel);
-    const uint32_t d2 = prmt(hd.x, 0u, 0x1010u), dmin2 = prmt(hd.x, 0u, 0x3232u);   // (d, d), (dmin, dmin)
+    const float d = half_lo_to_float(hd.x), dmin = half_hi_to_float(hd.x);
     KqRow r;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const uint32_t s = 0x4040u + 0x0101u * i;   // byte i, twice, with 0x64 high bytes
-        const uint32_t sc2 = hsub2(prmt(sc4, 0x64646464u, s), kH2_1024);
-        const uint32_t m2 = hsub2(prmt(m4, 0x64646464u, s), kH2_1024);
-        r.ds[i] = hmul2(d2, sc2);
-        r.ndm[i] = hmul2(dmin2, m2) ^ 0x80008000u;
+        r.ds[i] = d * static_cast<float>((sc4 >> (8 * i)) & 0xFFu);
+        r.ndm[i] = -dmin * static_cast<float>((m4 >> (8 * i)) & 0xFFu);
     }
     return r;
 }
@@ -101,7 +108,7 @@ __device__ __forceinline__ void kq_chunk(uint32_t blk, int gg, const KqRow &r, u
         h0 = lds128(blk + 16);
         h1 = lds128(blk + 32);
     }
-    const uint32_t ds = r.ds[gg], ndm = r.ndm[gg];
+    const float ds = r.ds[gg], ndm = r.ndm[gg];
     const uint32_t j = 2u * gg + h;   // sub-block (and qh bit) of these weights
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
@@ -133,8 +140,8 @@ __device__ __forceinline__ void kq_chunk(uint32_t blk, int gg, const KqRow &r, u
             q01 = hfma2(v01, kH2_1_16, kH2_m64);
             q23 = hfma2(v23, kH2_1_16, kH2_m64);
         }
-        out[2 * u] = hfma2(q01, ds, ndm);
-        out[2 * u + 1] = hfma2(q23, ds, ndm);
+        out[2 * u] = scale_pair(q01, ds, ndm);
+        out[2 * u + 1] = scale_pair(q23, ds, ndm);
     }
 }
 
@@ -150,12 +157,10 @@ __device__ __forceinline__ uint4 lds128_a2(uint32_t addr) {
 template <int h, bool ALIGNED = false>
 __device__ __forceinline__ void q6_chunk(uint32_t blk, int gg, uint32_t (&out)[16]) {
     const int hf = gg >> 1, t = 2 * (gg & 1) + h;
-    const uint32_t d = lds16(blk + 208);
-    const uint32_t d2 = d | (d << 16);
-    const uint32_t scb = lds16(blk + 192 + 8 * hf + 2 * t) ^ 0x8080u;   // sc[8hf+2t], sc[8hf+2t+1] (+128)
-    const uint32_t kH2_1152 = 0x64806480u;
-    const uint32_t ds0 = hmul2(d2, hsub2(prmt(scb, 0x64646464u, 0x4040u), kH2_1152));   // l < 16
-    const uint32_t ds1 = hmul2(d2, hsub2(prmt(scb, 0x64646464u, 0x4141u), kH2_1152));   // l >= 16
+    const float d = half_lo_to_float(lds16(blk + 208));
+    const uint32_t scb = lds16(blk + 192 + 8 * hf + 2 * t);   // sc[8hf+2t], sc[8hf+2t+1] (int8)
+    const float ds0 = d * static_cast<float>(static_cast<int8_t>(scb & 0xFFu));          // l < 16
+    const float ds1 = d * static_cast<float>(static_cast<int8_t>((scb >> 8) & 0xFFu));   // l >= 16
     const uint32_t qlo = 64 * hf + 32 * h, qho = 128 + 32 * hf;
     auto ld16 = [](uint32_t a) { return ALIGNED ? lds128(a) : lds128_a2(a); };
     const uint4 l0 = ld16(blk + qlo), l1 = ld16(blk + qlo + 16);
@@ -175,9 +180,9 @@ __device__ __forceinline__ void q6_chunk(uint32_t blk, int gg, uint32_t (&out)[1
         uint32_t v23 = and_or(l3, 0x000F000Fu, kH2_1024);
         v01 = or_and(v01, sh >= 0 ? (h2 << sh) : (h2 >> -sh), 0x00300030u);
         v23 = or_and(v23, sh >= 0 ? (h3 << sh) : (h3 >> -sh), 0x00300030u);
-        const uint32_t ds = u < 4 ? ds0 : ds1;
-        out[2 * u] = hmul2(hsub2(v01, kH2_1056), ds);
-        out[2 * u + 1] = hmul2(hsub2(v23, kH2_1056), ds);
+        const float ds = u < 4 ? ds0 : ds1;
+        out[2 * u] = scale_pair(hsub2(v01, kH2_1056), ds, 0.f);
+        out[2 * u + 1] = scale_pair(hsub2(v23, kH2_1056), ds, 0.f);
     }
 }
 
@@ -195,18 +200,17 @@ __device__ __forceinline__ void iq4_chunk(uint32_t blk, int gg, uint32_t (&out)[
     const int j = 2 * gg + h;
     const uint2 hd = lds64(blk);
     const uint32_t ls = ((hd.y >> (4 * j)) & 15u) | (((hd.x >> (16 + 2 * j)) & 3u) << 4);
-    const uint32_t d2 = prmt(hd.x, 0u, 0x1010u);
-    const uint32_t dl = hmul2(d2, hsub2(prmt(ls, 0x64646464u, 0x4040u), kH2_1056));   // d * (ls - 32)
+    const float dl = half_lo_to_float(hd.x) * static_cast<float>(static_cast<int>(ls) - 32);   // d * (ls - 32)
     const uint2 a = lds64(blk + 8 + 16 * j), b = lds64(blk + 16 + 16 * j);
     const uint32_t kH2_1152 = 0x64806480u;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
         const uint32_t w = u == 0 ? a.x : u == 1 ? a.y : u == 2 ? b.x : b.y;   // bytes p = 4u .. 4u+3
         const uint32_t r01 = iq4_lookup(w), r23 = iq4_lookup(w >> 16);
-        out[2 * u] = hmul2(hsub2(prmt(r01, 0x64646464u, 0x4240u), kH2_1152), dl);       // r = p, p+1
-        out[2 * u + 1] = hmul2(hsub2(prmt(r23, 0x64646464u, 0x4240u), kH2_1152), dl);   // p+2, p+3
-        out[8 + 2 * u] = hmul2(hsub2(prmt(r01, 0x64646464u, 0x4341u), kH2_1152), dl);   // p+16, p+17
-        out[9 + 2 * u] = hmul2(hsub2(prmt(r23, 0x64646464u, 0x4341u), kH2_1152), dl);   // p+18, p+19
+        out[2 * u] = scale_pair(hsub2(prmt(r01, 0x64646464u, 0x4240u), kH2_1152), dl, 0.f);       // r = p, p+1
+        out[2 * u + 1] = scale_pair(hsub2(prmt(r23, 0x64646464u, 0x4240u), kH2_1152), dl, 0.f);   // p+2, p+3
+        out[8 + 2 * u] = scale_pair(hsub2(prmt(r01, 0x64646464u, 0x4341u), kH2_1152), dl, 0.f);   // p+16, p+17
+        out[9 + 2 * u] = scale_pair(hsub2(prmt(r23, 0x64646464u, 0x4341u), kH2_1152), dl, 0.f);   // p+18, p+19
     }
 }
 
@@ -272,6 +276,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n0 = blockIdx.x * kRows;
     const int t0 = blockIdx.y * p.n_tile;
     const int nchunks = p.nsb * 4;
+    if constexpr (kBoundsChecks) {   // rings, barriers and TMEM columns inside their budgets
+        uint32_t dyn;
+        asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+        const bool lay = misc_off + 8u + (base - raw) <= dyn && static_cast<uint32_t>(BS) * p.b_stage_bytes <= p.q_off &&
+                         p.q_off + static_cast<uint32_t>(QS) * p.q_stage_bytes <= p.bar_off &&
+                         p.q_stage_bytes >= kRows * p.row_pitch && p.row_pitch >= static_cast<uint32_t>(p.S * p.bb) &&
+                         static_cast<uint32_t>(p.n_tile) <= p.a_col && AS <= kMaxASlots &&
+                         p.a_col + static_cast<uint32_t>(AS) * kASlotCols <= kTmemCols &&
+                         p.b_stage_bytes >= static_cast<uint32_t>(p.xk * p.n_tile) * 128u;
+        if (!in_bounds(lay, p.status)) return;
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < QS; ++s) {
@@ -327,6 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   // arithmetic wraps modulo 2^32 and keeps the low four bits)
                 blk += ((static_cast<uint32_t>(row) * static_cast<uint32_t>(p.nsb) + static_cast<uint32_t>(sb - j)) *
                         static_cast<uint32_t>(p.bb)) & 15u;
+            if (!in_bounds(blk + static_cast<uint32_t>(p.bb) <= stage + (r + 1) * p.row_pitch, p.status))
+                blk = stage + r * p.row_pitch;   // bounds check failed: decode the row's first block instead
             KqRow kr{};
             if constexpr (TYPE == 12 || TYPE == 13) kr = kq_row(blk, h);
             ok = wait_or_abort(aempty(sa), aph ^ 1u, abort_flag, p.status);
@@ -415,9 +432,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tail_src = p.W + t16;
                             tail_dst = st + rr * p.row_pitch + static_cast<uint32_t>(t16 - lo);
                         }
-                        src[i] = p.W + lo;
-                        dst[i] = st + rr * p.row_pitch;
-                        nb[i] = static_cast<uint32_t>(hi - lo);
+                        const int64_t end = o + static_cast<int64_t>(ns) * p.bb;
+                        if (in_bounds(lo >= 0 && end <= p.total_bytes && (end + 15 - lo) / 16 * 16 <= p.row_pitch,
+                                      p.status)) {
+                            src[i] = p.W + lo;
+                            dst[i] = st + rr * p.row_pitch;
+                            nb[i] = static_cast<uint32_t>(hi - lo);
+                        } else {
+                            tail_len = 0;
+                        }
                     }
                     my += nb[i];
                 }

@@ -353,6 +353,15 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
     const uint32_t xexp = xreg + p.x_tx, xsums = xexp + kM1Sb * p.kw;
     const uint32_t ring = base + p.ring_offset + warp * D * p.slot_bytes;
 
+    const uint32_t ring_end = base + p.ring_offset + (blockDim.x >> 5) * D * p.slot_bytes;
+    if constexpr (kBoundsChecks) {   // the layout inside the launch's dynamic shared memory
+        uint32_t dyn;
+        asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+        const bool lay = ring_end - smem_u32(smem) <= dyn && p.red_offset >= scratch_offset(blockDim.x >> 5, D) &&
+                         p.x_offset >= p.red_offset && p.ring_offset >= p.x_offset + (blockDim.x >> 5) * p.x_warp_bytes &&
+                         (!XRES || p.x_tx <= p.x_warp_bytes) && p.w_bytes + (XRES ? 0u : p.x_bytes) <= p.slot_bytes;
+        if (!in_bounds(lay, p.status)) return;
+    }
     const int G = gridDim.x, b = blockIdx.x;
     const int T = p.tile0[p.nproj];   // row tiles of all projections; CTA b owns [T b / G, T (b+1) / G)
     const int t_begin = static_cast<int>(static_cast<int64_t>(T) * b / G);
@@ -401,9 +410,15 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
         const uint32_t xtx = XRES ? 0u : p.x_tx;
         if constexpr (TMA) {
             if (lane == 0) {
-                mbar_arrive_expect_tx(bar, p.w_bytes + xtx);
-                tma_load_2d(wslot(s), &wmaps.m[j], sb * (BB / 8), row0, bar);
-                if (!XRES) tma_load_3d(xslot(s), &xmap, 0, sb * 4, 0, bar);
+                if (in_bounds(s < D && wslot(s) + p.w_bytes <= ring + (s + 1) * p.slot_bytes && sb < p.nsb &&
+                                  (XRES || xslot(s) + xtx <= wslot(s)),
+                              p.status)) {
+                    mbar_arrive_expect_tx(bar, p.w_bytes + xtx);
+                    tma_load_2d(wslot(s), &wmaps.m[j], sb * (BB / 8), row0, bar);
+                    if (!XRES) tma_load_3d(xslot(s), &xmap, 0, sb * 4, 0, bar);
+                } else {
+                    mbar_arrive(bar);
+                }
             }
         } else {
             const int ns = min(S, kb1 - sb);
@@ -423,9 +438,16 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
                     tail_len = static_cast<int>(o + static_cast<int64_t>(ns) * BB - t16);
                     tail_off = static_cast<uint32_t>(t16 - lo);
                 }
-                src = W + lo;
-                dst = wslot(s) + lane * p.row_pitch;
-                nbytes = static_cast<uint32_t>(hi - lo);
+                const int64_t end = o + static_cast<int64_t>(ns) * BB;
+                if (in_bounds(lo >= 0 && end <= p.total_bytes[j] && (end + 15 - lo) / 16 * 16 <= p.row_pitch &&
+                                  wslot(s) + (lane + 1) * p.row_pitch <= ring + (s + 1) * p.slot_bytes,
+                              p.status)) {
+                    src = W + lo;
+                    dst = wslot(s) + lane * p.row_pitch;
+                    nbytes = static_cast<uint32_t>(hi - lo);
+                } else {
+                    tail_len = 0;
+                }
             }
             if (tail_len > 0) {
                 uint8_t *gd = smem + (dst + tail_off - smem_u32(smem));
@@ -601,7 +623,16 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
                     base_a += ((static_cast<uint32_t>(ra) * nsb + sbu) * static_cast<uint32_t>(BB)) & 15u;
                     base_b += ((static_cast<uint32_t>(rb) * nsb + sbu) * static_cast<uint32_t>(BB)) & 15u;
                 }
-                if constexpr (M1) {
+                // the stage's blocks inside its slot; the x it pairs with inside this warp's x region
+                const uint32_t span = static_cast<uint32_t>(ns) * BB, xsbe = xsb0 + static_cast<uint32_t>(ns);
+                const uint32_t x_end = M1 ? xexp + xsbe * kM1Sb : xst + (tok * xrows + 4u * xsbe) * 128u;
+                const uint32_t x_lim = XRES ? xreg + p.x_tx : xst + p.x_bytes;
+                const bool stage_ok = in_bounds(ns >= 1 && base_b + span <= wst + p.w_bytes && base_a + span <= wst + p.w_bytes &&
+                                                    (M1 ? x_end <= xsums && xsums + 32u * xsbe <= xreg + p.x_warp_bytes
+                                                        : x_end <= x_lim),
+                                                p.status);
+                if (!stage_ok) {
+                } else if constexpr (M1) {
                     const uint32_t slot = ((g >> 1) == c) ? 8u * g : 64u;   // B of column g, or the zero slot
 #pragma unroll 2
                     for (int j = 0; j < ns; ++j) {
@@ -636,7 +667,13 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
         // This warp's partial of tile t goes to its slot of the current round (tokens < M only);
         // warps run on without waiting for each other.
         float *pt = red + ((t - round0) * p.ks + kidx) * 16 * p.M;
-        if constexpr (M1) {   // the four lanes of a row group hold its four sub-block pairs
+        if (!in_bounds(t - round0 < p.round_tiles && kidx < p.ks &&
+                           p.red_offset + 4u * static_cast<uint32_t>(((t - round0 + 1) * p.ks) * 16 * p.M) <= p.x_offset,
+                       p.status))
+            pt = nullptr;   // bounds check failed: the partial is not stored
+        if (!pt) {
+            acc1[0] = acc1[1] = 0.f;
+        } else if constexpr (M1) {   // the four lanes of a row group hold its four sub-block pairs
             float a0 = acc1[0], a1 = acc1[1];
             a0 += __shfl_xor_sync(0xFFFFFFFFu, a0, 1);
             a1 += __shfl_xor_sync(0xFFFFFFFFu, a1, 1);
@@ -651,7 +688,7 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
             pt[2 * c * 16 + g] = acc[0];
             pt[2 * c * 16 + g + 8] = acc[2];
         }
-        if (2 * c + 1 < p.M) {
+        if (pt && 2 * c + 1 < p.M) {
             pt[(2 * c + 1) * 16 + g] = acc[1];
             pt[(2 * c + 1) * 16 + g + 8] = acc[3];
         }

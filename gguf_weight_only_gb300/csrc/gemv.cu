@@ -112,7 +112,9 @@ struct GemvArgs {
     uint32_t slot_bytes;     // one ring slot, rounded to 1 KB
     uint32_t red_offset, x_offset, ring_offset;
     int round_tiles;         // row tiles whose partials are reduced together (one barrier pair)
-    int m1;                  // single-token K-quant kernel (sub-blocks on the MMA's n side)
+    int m1;                  // single-token kernel (sub-blocks on the MMA's n side)
+    uint32_t lut_offset;     // single-token IQ4_XS: the replicated codebook byte table
+    int qswap;               // single-token K-quants: odd-c lanes read their quant halves swapped
 };
 
 // Weight tensor maps, one per projection (unused entries stay zero).
@@ -145,7 +147,7 @@ constexpr uint32_t kM1Rec = 72, kM1Sb = 16 * kM1Rec;   // record and superblock 
 
 // Builds the staged B records and the sub-block sums from the warp's x tile (M = 1: row
 // r = 4 b + segment of 128 bytes, chunk p of row r stored at p ^ (r & 7)).
-__device__ __forceinline__ void m1_stage(uint32_t xtile, uint32_t xexp, uint32_t xsums, int kw, int lane) {
+__device__ __forceinline__ void m1_stage(uint32_t xtile, uint32_t xexp, uint32_t xsums, int kw, int lane, int qswap) {
     const uint32_t nitems = 64u * static_cast<uint32_t>(kw);   // (superblock, sub-block, word): a multiple of 32
     for (uint32_t q = lane; q < nitems; q += 32) {
         const uint32_t u = q & 7u, j = (q >> 3) & 7u, b = q >> 6;
@@ -153,7 +155,10 @@ __device__ __forceinline__ void m1_stage(uint32_t xtile, uint32_t xexp, uint32_t
         const uint32_t r = 4u * b + (k >> 6), col = k & 63u;
         const uint2 v = lds64(xtile + r * 128u + ((((col >> 3) ^ (r & 7u))) << 4) + ((col & 4u) << 1));
         const uint32_t p02 = prmt(v.x, v.y, 0x5410u), p13 = prmt(v.x, v.y, 0x7632u);   // (x0, x2), (x1, x3)
-        const uint32_t e = xexp + b * kM1Sb + (2u * u) * kM1Rec + 8u * j;   // records 2u and 2u+1, slot j
+        // records 2u and 2u+1, slot j (the records of word u ^ 4 when the column's carrier reads
+        // its quant halves swapped)
+        const uint32_t us = u ^ ((qswap && ((j >> 1) & 1u)) ? 4u : 0u);
+        const uint32_t e = xexp + b * kM1Sb + (2u * us) * kM1Rec + 8u * j;
         if (j & 1u) {
             sts64(e, 0u, p02);
             sts64(e + kM1Rec, 0u, p13);
@@ -161,7 +166,7 @@ __device__ __forceinline__ void m1_stage(uint32_t xtile, uint32_t xexp, uint32_t
             sts64(e, p02, 0u);
             sts64(e + kM1Rec, p13, 0u);
         }
-        if (j == 0u) {   // the zero slots of records 2u, 2u+1
+        if (j == 0u) {   // the zero slots of records 2u, 2u+1 (column 0 is never swapped)
             sts64(e + 64u, 0u, 0u);
             sts64(e + kM1Rec + 64u, 0u, 0u);
         }
@@ -178,20 +183,25 @@ __device__ __forceinline__ void m1_stage(uint32_t xtile, uint32_t xexp, uint32_t
 // One superblock of rows g, g+8 for the single-token path: acc[0] (row g) and acc[1] (row
 // g+8) gain this lane's two sub-blocks. bx = the lane's slot in the superblock's first staged
 // record, sums = the superblock's eight fp32 sub-block sums of x.
+// swap16 = 16 for lanes that read their 32-byte quant group as (second, first) half: with a stage
+// pitch of 32 or 96 (mod 128) bytes rows g and g+1 sit 2 or 6 bank groups apart and the lanes of
+// odd c then fill the bank groups the even ones leave (4 wavefronts per 16-byte load instead of
+// 8); the staged records of their columns are stored in the same order.
 template <int TYPE>
 __device__ __forceinline__ void superblock_kq_m1(uint32_t blk_a, uint32_t blk_b, uint32_t bx, uint32_t sums, int c,
-                                                 float (&acc)[2]) {
+                                                 uint32_t swap16, float (&acc)[2]) {
     constexpr bool Q5 = (TYPE == 13);
     constexpr uint32_t QS = Q5 ? 48 : 16;
     const uint4 ha = lds128(blk_a), hb = lds128(blk_b);
-    const uint4 qa0 = lds128(blk_a + QS + 32 * c), qa1 = lds128(blk_a + QS + 32 * c + 16);
-    const uint4 qb0 = lds128(blk_b + QS + 32 * c), qb1 = lds128(blk_b + QS + 32 * c + 16);
+    const uint32_t q0 = QS + 32 * c + swap16, q1 = QS + 32 * c + (16u - swap16);
+    const uint4 qa0 = lds128(blk_a + q0), qa1 = lds128(blk_a + q1);
+    const uint4 qb0 = lds128(blk_b + q0), qb1 = lds128(blk_b + q1);
     uint4 ha0 = make_uint4(0, 0, 0, 0), ha1 = ha0, hb0 = ha0, hb1 = ha0;
     if constexpr (Q5) {
-        ha0 = lds128(blk_a + 16);
-        ha1 = lds128(blk_a + 32);
-        hb0 = lds128(blk_b + 16);
-        hb1 = lds128(blk_b + 32);
+        ha0 = lds128(blk_a + 16 + swap16);
+        ha1 = lds128(blk_a + 32 - swap16);
+        hb0 = lds128(blk_b + 16 + swap16);
+        hb1 = lds128(blk_b + 32 - swap16);
     }
     float d1[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
     const uint32_t rl = (4u - 2u * c) & 31u, rh = (7u - 2u * c) & 31u;   // Q5_K: bit 2c -> bit 4, 2c+1 -> bit 8
@@ -242,6 +252,107 @@ __device__ __forceinline__ void superblock_kq_m1(uint32_t blk_a, uint32_t blk_b,
     constexpr float k24 = 16777216.0f, k20 = 1048576.0f;   // 2^24, 2^20
     acc[0] += da * (sa0 * k24 * (d1[0] + e1[0]) + sa1 * k20 * (d1[1] + e1[1])) - dma * (ma0 * xs0 + ma1 * xs1);
     acc[1] += db * (sb0 * k24 * (d1[2] + e1[2]) + sb1 * k20 * (d1[3] + e1[3])) - dmb * (mb0 * xs0 + mb1 * xs1);
+}
+
+// ---------------------------------------------------------------- single-token IQ4_XS path
+//
+// IQ4_XS takes the same column scheme with the codebook lookup moved into shared memory: a table
+// of the 256 quant bytes whose entry is the fp16 pair (kv[b & 15], kv[b >> 4]) (exact integers,
+// so D[row][j] is the unscaled sum over sub-block j of kv * x and d (ls_j - 32) is applied once
+// per sub-block in fp32). The table is replicated 32 times and lane l reads copy l (entry b of
+// copy l at b * 128 + 4 l, always bank l): one conflict-free 32-bit load per quant byte replaces
+// the byte-permute lookup, moving the decode's cost from the integer pipe to shared memory.
+// Quant byte p of a sub-block holds weights p (low nibble) and p + 16 (high nibble), so a table
+// entry is the A pair of one k-slot pair and the staged B holds (x_p, x_{p+16}).
+//
+// Lane (g, c) decodes qs bytes 32c .. 32c+31 of rows g, g+8 (words w = 0..3: sub-block 2c,
+// 4..7: 2c+1), reading its four 8-byte chunks in the order i ^ c: at step u it holds word
+// w = u ^ 2c, which spreads a warp's chunk loads over all banks (two wavefronts each) at every
+// stage pitch but those of 64 mod 128 bytes. MMA (u, h) takes bytes 2h, 2h+1 of that word:
+// a0 / a1 = the entries of byte 2h of rows g / g+8, a2 / a3 = byte 2h+1. Record (b, 2u + h)
+// holds in slot j, for the four columns the lanes carry at step u, the pairs (x[p], x[p+16]),
+// (x[p+1], x[p+17]) with p = 32j + 4(w & 3) + 2h and w = u ^ 2(j >> 1); its other four slots
+// and slot 8 are zero.
+constexpr uint32_t kIq4LutBytes = 256u * 128u;
+
+// Codebook value kv[i] (the IQ4 tables hold kv + 128 bytes).
+__device__ __forceinline__ int iq4_kv(uint32_t i) {
+    const uint32_t t = (i < 4) ? kIq4T0 : (i < 8) ? kIq4T1 : (i < 12) ? kIq4T2 : kIq4T3;
+    return static_cast<int>((t >> (8u * (i & 3u))) & 0xFFu) - 128;
+}
+
+// All threads of the CTA fill the table (run before the dependency wait: it is constant).
+__device__ __forceinline__ void iq4_lut_fill(uint32_t lut) {
+    for (uint32_t i = threadIdx.x; i < 256u * 32u; i += blockDim.x) {
+        const uint32_t b = i >> 5, l = i & 31u;
+        const uint32_t lo = __half_as_ushort(__int2half_rn(iq4_kv(b & 15u)));
+        const uint32_t hi = __half_as_ushort(__int2half_rn(iq4_kv(b >> 4)));
+        sts32(lut + b * 128u + 4u * l, lo | (hi << 16));
+    }
+}
+
+// The staged B records of the IQ4_XS single-token path from the warp's x tile (M = 1, row
+// r = 4 b + segment, chunk p of row r stored at p ^ (r & 7)); item (b, j, word w & 3) writes
+// slot j of records 2u, 2u+1 (u = w ^ 2 (j >> 1), the step at which its carrier holds word w)
+// and zeros slot j ^ 1 of both (and slot 8 when j < 2).
+__device__ __forceinline__ void m1_stage_iq4(uint32_t xtile, uint32_t xexp, int kw, int lane) {
+    const uint32_t nitems = 32u * static_cast<uint32_t>(kw);   // a multiple of 32
+    auto x4 = [&](uint32_t b, uint32_t k) {   // x[k .. k+3] of superblock b (k % 4 == 0)
+        const uint32_t r = 4u * b + (k >> 6), col = k & 63u;
+        return lds64(xtile + r * 128u + ((((col >> 3) ^ (r & 7u))) << 4) + ((col & 4u) << 1));
+    };
+    for (uint32_t q = lane; q < nitems; q += 32) {
+        const uint32_t uq = q & 3u, j = (q >> 2) & 7u, b = q >> 5;
+        const uint32_t w4 = uq + 4u * (j & 1u), u = w4 ^ (2u * (j >> 1)), k = 32u * j + 4u * uq;
+        const uint2 v = x4(b, k), w = x4(b, k + 16u);   // x[k..k+3], x[k+16..k+19]
+        const uint32_t e = xexp + b * kM1Sb + (2u * u) * kM1Rec;
+        sts64(e + 8u * j, prmt(v.x, w.x, 0x5410u), prmt(v.x, w.x, 0x7632u));                   // h = 0
+        sts64(e + kM1Rec + 8u * j, prmt(v.y, w.y, 0x5410u), prmt(v.y, w.y, 0x7632u));          // h = 1
+        sts64(e + 8u * (j ^ 1u), 0u, 0u);
+        sts64(e + kM1Rec + 8u * (j ^ 1u), 0u, 0u);
+        if (j < 2u) {
+            sts64(e + 64u, 0u, 0u);
+            sts64(e + kM1Rec + 64u, 0u, 0u);
+        }
+    }
+}
+
+// One IQ4_XS superblock of rows g, g+8 for the single-token path: acc[0] (row g) and acc[1]
+// (row g+8) gain this lane's sub-blocks 2c, 2c+1. bx_lo / bx_hi = the lane's slot in the
+// superblock's first record for steps 0-3 / 4-7 (the column it carries then, or the zero
+// slot); lutl = this lane's copy of the byte table.
+__device__ __forceinline__ void superblock_iq4_m1(uint32_t blk_a, uint32_t blk_b, uint32_t bx_lo, uint32_t bx_hi,
+                                                  uint32_t lutl, int c, float (&acc)[2]) {
+    const uint2 ha = lds64(blk_a), hb = lds64(blk_b);
+    uint2 qa[4], qb[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        qa[i] = lds64(blk_a + 8 + 32 * c + 8 * (i ^ c));
+        qb[i] = lds64(blk_b + 8 + 32 * c + 8 * (i ^ c));
+    }
+    float d1[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
+    auto entry = [&](uint32_t w, uint32_t k) { return lds32(lutl + 128u * prmt(w, 0u, 0x4440u | k)); };
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const uint32_t wa = (u & 1) ? qa[u >> 1].y : qa[u >> 1].x, wb = (u & 1) ? qb[u >> 1].y : qb[u >> 1].x;
+        const uint32_t bx = u < 4 ? bx_lo : bx_hi;
+        const uint2 B0 = lds64(bx + (2u * u) * kM1Rec), B1 = lds64(bx + (2u * u + 1u) * kM1Rec);
+        mma16816(d1, entry(wa, 0), entry(wb, 0), entry(wa, 1), entry(wb, 1), B0.x, B0.y);
+        mma16816(e1, entry(wa, 2), entry(wb, 2), entry(wa, 3), entry(wb, 3), B1.x, B1.y);
+    }
+    // ls of sub-blocks 2c, 2c+1: low nibble from scales_l (bytes 4..7 of the block), high two
+    // bits from scales_h (bytes 2, 3)
+    auto ls_pair = [&](const uint2 &h, float &l0, float &l1) {
+        const uint32_t lo = (h.y >> (8 * c)) & 0xFFu, hi2 = (h.x >> (16 + 4 * c)) & 0xFu;
+        l0 = static_cast<float>(static_cast<int>((lo & 15u) | ((hi2 & 3u) << 4)) - 32);
+        l1 = static_cast<float>(static_cast<int>((lo >> 4) | ((hi2 >> 2) << 4)) - 32);
+    };
+    float la0, la1, lb0, lb1;
+    ls_pair(ha, la0, la1);
+    ls_pair(hb, lb0, lb1);
+    const float da = half_lo_to_float(ha.x), db = half_lo_to_float(hb.x);
+    acc[0] += da * (la0 * (d1[0] + e1[0]) + la1 * (d1[1] + e1[1]));
+    acc[1] += db * (lb0 * (d1[2] + e1[2]) + lb1 * (d1[3] + e1[3]));
 }
 
 // ---------------------------------------------------------------- fused prologues
@@ -336,7 +447,8 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
     constexpr int BB = GemvFmt<TYPE>::BB;
     constexpr bool PERM = XRES && TYPE != 23 && !M1;   // resident x is permuted once for the K-quant/Q6_K pairing
     constexpr bool XSUM = XRES && (TYPE == 12 || TYPE == 13) && !M1;   // staged sub-block sums of x (min term)
-    static_assert(!M1 || (XRES && (TYPE == 12 || TYPE == 13)), "single-token path: K-quants, resident x");
+    static_assert(!M1 || (XRES && (TYPE == 12 || TYPE == 13 || TYPE == 23)),
+                  "single-token path: K-quants and IQ4_XS, resident x");
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
@@ -359,7 +471,8 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
         asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
         const bool lay = ring_end - smem_u32(smem) <= dyn && p.red_offset >= scratch_offset(blockDim.x >> 5, D) &&
                          p.x_offset >= p.red_offset && p.ring_offset >= p.x_offset + (blockDim.x >> 5) * p.x_warp_bytes &&
-                         (!XRES || p.x_tx <= p.x_warp_bytes) && p.w_bytes + (XRES ? 0u : p.x_bytes) <= p.slot_bytes;
+                         (!XRES || p.x_tx <= p.x_warp_bytes) && p.w_bytes + (XRES ? 0u : p.x_bytes) <= p.slot_bytes &&
+                         (!(M1 && TYPE == 23) || (p.lut_offset >= p.red_offset && p.lut_offset + kIq4LutBytes <= p.x_offset));
         if (!in_bounds(lay, p.status)) return;
     }
     const int G = gridDim.x, b = blockIdx.x;
@@ -478,6 +591,10 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
     };
     if constexpr (XRES) {
         for (int s = 0; s < D && s < total; ++s) issue_next(s);
+        if constexpr (M1 && TYPE == 23) {   // the codebook table: constant, built before the wait
+            iq4_lut_fill(base + p.lut_offset);
+            __syncthreads();
+        }
         pdl_wait();
         float *const sq = reinterpret_cast<float *>(gbase + scratch_offset(blockDim.x >> 5, D));   // [warp][token]
         if (PRO && p.pro == 2) {
@@ -586,7 +703,8 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
             __syncwarp();
         }
         if constexpr (M1) {   // after the tile is complete (copied, or filled by a prologue)
-            m1_stage(xreg, xexp, xsums, p.kw, lane);
+            if constexpr (TYPE == 23) m1_stage_iq4(xreg, xexp, p.kw, lane);
+            else m1_stage(xreg, xexp, xsums, p.kw, lane, p.qswap);
             __syncwarp();
         }
     } else {
@@ -628,17 +746,29 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
                 const uint32_t x_end = M1 ? xexp + xsbe * kM1Sb : xst + (tok * xrows + 4u * xsbe) * 128u;
                 const uint32_t x_lim = XRES ? xreg + p.x_tx : xst + p.x_bytes;
                 const bool stage_ok = in_bounds(ns >= 1 && base_b + span <= wst + p.w_bytes && base_a + span <= wst + p.w_bytes &&
-                                                    (M1 ? x_end <= xsums && xsums + 32u * xsbe <= xreg + p.x_warp_bytes
+                                                    (M1 ? x_end <= xsums && (TYPE == 23 || xsums + 32u * xsbe <= xreg + p.x_warp_bytes)
                                                         : x_end <= x_lim),
                                                 p.status);
                 if (!stage_ok) {
+                } else if constexpr (M1 && TYPE == 23) {
+                    // B of column g when this lane carries it at steps 0-3 (column 2c for c < 2, 2c+1
+                    // for c >= 2: the chunk order i ^ c swaps the halves) or steps 4-7 (the other)
+                    const int ja = 2 * c + (c >= 2 ? 1 : 0), jb = 2 * c + (c >= 2 ? 0 : 1);
+                    const uint32_t slot_lo = (g == ja) ? 8u * g : 64u, slot_hi = (g == jb) ? 8u * g : 64u;
+                    const uint32_t lutl = base + p.lut_offset + 4u * static_cast<uint32_t>(lane);
+#pragma unroll 2
+                    for (int j = 0; j < ns; ++j) {
+                        const uint32_t rb = xexp + (xsb0 + j) * kM1Sb;
+                        superblock_iq4_m1(base_a + j * BB, base_b + j * BB, rb + slot_lo, rb + slot_hi, lutl, c, acc1);
+                    }
                 } else if constexpr (M1) {
                     const uint32_t slot = ((g >> 1) == c) ? 8u * g : 64u;   // B of column g, or the zero slot
+                    const uint32_t swap16 = (p.qswap && (c & 1)) ? 16u : 0u;
 #pragma unroll 2
                     for (int j = 0; j < ns; ++j) {
                         const uint32_t b = xsb0 + j;
                         superblock_kq_m1<TYPE>(base_a + j * BB, base_b + j * BB, xexp + b * kM1Sb + slot,
-                                               xsums + 32u * b, c, acc1);
+                                               xsums + 32u * b, c, swap16, acc1);
                     }
                 } else {
 #pragma unroll 2   // two superblocks' independent decode chains can interleave
@@ -810,7 +940,7 @@ GemvPlan make_plan(int type, int64_t T, int64_t K, int M, int num_sms, bool need
         o.x_tx = static_cast<uint32_t>(M * (xres ? kw : S) * 512);
         o.x_bytes = xres ? 0u : o.x_tx;
         const uint32_t xsum_bytes = (type == 12 || type == 13) ? static_cast<uint32_t>(M * kw * 32) : 0u;
-        const uint32_t m1_bytes = m1 ? static_cast<uint32_t>(kw * (16 * 72) + kw * 32) : 0u;
+        const uint32_t m1_bytes = m1 ? static_cast<uint32_t>(kw * (16 * 72) + (type == 23 ? 0 : kw * 32)) : 0u;
         o.x_warp_bytes = xres ? ((o.x_tx + (m1 ? m1_bytes : xsum_bytes) + 1023u) & ~1023u) : 0u;
         // a slot that also holds a 128-byte-swizzled x tile starts on 1 KB, weights alone on 128 B
         o.slot_bytes = xres ? ((o.w_bytes + 127u) & ~127u) : ((o.x_bytes + o.w_bytes + 1023u) & ~1023u);
@@ -818,7 +948,9 @@ GemvPlan make_plan(int type, int64_t T, int64_t K, int M, int num_sms, bool need
         const uint32_t bars = (scratch_offset(w, D) + kScratchBytes + 1023u) & ~1023u;
         o.red_offset = bars;
         o.round_tiles = round_tiles;
-        o.x_offset = (bars + static_cast<uint32_t>(round_tiles * ks * 16 * M * sizeof(float)) + 1023u) & ~1023u;
+        o.lut_offset = (bars + static_cast<uint32_t>(round_tiles * ks * 16 * M * sizeof(float)) + 1023u) & ~1023u;
+        const uint32_t lut_bytes = (m1 && type == 23) ? kIq4LutBytes : 0u;
+        o.x_offset = o.lut_offset + lut_bytes;
         o.ring_offset = o.x_offset + w * o.x_warp_bytes;
         return static_cast<size_t>(1024) + o.ring_offset + static_cast<size_t>(w) * D * o.slot_bytes;
     };
@@ -847,6 +979,10 @@ GemvPlan make_plan(int type, int64_t T, int64_t K, int M, int num_sms, bool need
     }
     a.K = static_cast<int>(K);
     a.m1 = m1 ? 1 : 0;
+    {
+        const uint32_t delta = (a.row_pitch % 128u) / 16u;   // bank-group shift from row g to row g + 1
+        a.qswap = (m1 && (type == 12 || type == 13) && (delta == 2u || delta == 6u)) ? 1 : 0;
+    }
     a.M = M;
     a.nsb = nsb;
     a.kw = kw;
@@ -880,8 +1016,8 @@ cudaError_t launch_t(const GemvMaps &wm, const CUtensorMap &xm, const GemvArgs &
 template <int TYPE>
 cudaError_t launch_type(bool tma, bool xres, const GemvMaps &wm, const CUtensorMap &xm, const GemvArgs &a,
                         int grid, int threads, size_t smem, bool pdl, cudaStream_t st) {
-    if constexpr (TYPE == 12 || TYPE == 13) {
-        if (a.m1) {   // single token, K-quants, x resident and rows copied by 2-D tensor copies
+    if constexpr (TYPE == 12 || TYPE == 13 || TYPE == 23) {
+        if (a.m1) {   // single token, x resident and rows copied by 2-D tensor copies
             if (!xres || !tma) return cudaErrorInvalidValue;
             if (a.best) return launch_t<TYPE, true, true, false, false, true, true>(wm, xm, a, grid, threads, smem, pdl, st);
             if (a.pro != 0) return launch_t<TYPE, true, true, false, true, false, true>(wm, xm, a, grid, threads, smem, pdl, st);
@@ -915,6 +1051,15 @@ cudaError_t launch_type(bool tma, bool xres, const GemvMaps &wm, const CUtensorM
 
 namespace {
 
+// QL_GEMV_M1_IQ4=0: IQ4_XS single tokens on the general kernel (A/B measurement).
+bool iq4_single_token_off() {
+    static const bool off = [] {
+        const char *e = std::getenv("QL_GEMV_M1_IQ4");
+        return e && e[0] == '0';
+    }();
+    return off;
+}
+
 // QL_GEMV_M1=0 selects the general kernel for single tokens as well (A/B measurement).
 bool single_token_off() {
     static const bool off = [] {
@@ -946,7 +1091,8 @@ cudaError_t launch_impl(int type, int nproj, const GemvProj *proj, const __half 
     // so a prologue or the greedy head sums exactly as the plain call does.
     const int64_t grid = std::min<int64_t>(num_sms > 0 ? num_sms : 1, T);
     const int64_t per_warp = (T + grid - 1) / grid * ((K / 256 + 7) / 8);   // tiles per CTA x superblocks per slice of 8
-    bool m1 = M == 1 && (type == 12 || type == 13) && per_warp >= 8 && !single_token_off();
+    const bool m1_type = type == 12 || type == 13 || (type == 23 && (K / 256) % 2 == 0 && !iq4_single_token_off());
+    bool m1 = M == 1 && m1_type && per_warp >= 8 && !single_token_off();
     GemvPlan pl = make_plan(type, T, K, M, num_sms, pro != 0 || head, m1);
     if (m1 && pl.smem > 227 * 1024) {
         m1 = false;

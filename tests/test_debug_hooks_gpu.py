@@ -50,11 +50,13 @@ def child(code: str, **env) -> dict:
 
 # one small case per kernel path: (entry, type, N, K, M)
 DEBUG_CASES = [
-    ("qlinear", 12, 300, 5120, 1),     # streaming decode, single-token path, 2-D tensor copies
-    ("qlinear", 13, 129, 2560, 1),     # streaming decode, single-token Q5_K
-    ("qlinear", 23, 300, 5120, 1),     # streaming decode, tokens-on-n path (IQ4_XS)
-    ("qlinear", 14, 129, 2560, 3),     # streaming decode, per-row bulk copies (Q6_K)
-    ("qlinear", 12, 64, 4096, 8),      # streaming decode, eight tokens
+    ("qlinear", 12, 300, 5120, 1),     # decode, 2-D tensor copies
+    ("qlinear", 13, 129, 2560, 1),     # decode, Q5_K
+    ("qlinear", 23, 300, 5120, 1),     # decode, tokens-on-n path (IQ4_XS)
+    ("qlinear", 14, 129, 2560, 3),     # decode, per-row bulk copies (Q6_K)
+    ("qlinear", 12, 64, 4096, 8),      # eight tokens
+    ("qlinear", 12, 8000, 4096, 1),    # persistent decode kernel, single-token K-quant path
+    ("qlinear", 23, 9728, 8192, 1),    # persistent decode kernel, single-token IQ4_XS path (codebook table)
     ("multi", 12, 64, 1024, 2),        # persistent decode kernel (projection set)
     ("silu", 12, 96, 1024, 1),         # persistent decode kernel, fused prologue
     ("qlinear", 12, 256, 2048, 100),   # tcgen05 prefill GEMM

@@ -243,9 +243,9 @@ def test_gemv_x_per_stage_matches_oracle(ql, t, N, K, M):
 # On 152 SMs the last four keep each warp's K slice (1 or 2 superblocks) in one stage and its
 # B operand in registers: slices of 2 (K=4096), of 1 (K=256), and of 2 with a last slice of 1
 # (K=1792: 2+2+2+1, K=768: 2+1).
-@pytest.mark.parametrize("t", (12, 13))
+@pytest.mark.parametrize("t", (12, 13, 23))
 @pytest.mark.parametrize("N,K", [(4100, 8192), (2432, 16384), (8000, 4096), (20000, 256), (24000, 1792),
-                                 (29184, 768)])
+                                 (29184, 768), (9728, 5120)])
 def test_single_token_kernel_matches_oracle(ql, t, N, K):
     W = synth.weights(t, N, K, [520, t, N, K])
     x = synth.activations(1, K, [521, t, K])

@@ -493,50 +493,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------------------------------------------- MMA issuer (warp 10)
-        if (lane == 0) {
-            const uint32_t idesc = idesc_f16_f32(kRows, p.n_tile);
-            bool ok = true;
-            const uint32_t box_bytes = static_cast<uint32_t>(p.n_tile) * 128u;
-            int sa = 0, xi = 0, sbb = 0;   // A slot, chunk within the x stage, x stage
-            uint32_t aph = 0, bph = 0;
-            for (int sb = 0; sb < p.nsb && ok; ++sb) {
-                if (!wait_or_abort(afull(sa), aph, abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t a0 = tmem + p.a_col + sa * kASlotCols;
+        // The whole warp runs the loop on warp-uniform values and one elected lane (always
+        // lane 0 of the converged warp, so the commits track its MMAs) issues. Measured on
+        // GB300 beside eight ALU-bound warps: an n = 32 MMA issues every ~35 cycles this way
+        // against ~85 from a branch that only lane 0 enters.
+        const uint32_t idesc = idesc_f16_f32(kRows, p.n_tile);
+        bool ok = true;
+        const uint32_t box_bytes = static_cast<uint32_t>(p.n_tile) * 128u;
+        int sa = 0, xi = 0, sbb = 0;   // A slot, chunk within the x stage, x stage
+        uint32_t aph = 0, bph = 0;
+        for (int sb = 0; sb < p.nsb && ok; ++sb) {
+            ok = __all_sync(0xFFFFFFFFu, wait_or_abort(afull(sa), aph, abort_flag, p.status));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t a0 = tmem + p.a_col + sa * kASlotCols;
 #pragma unroll
-                for (int gg = 0; gg < 4; ++gg) {
-                    if (xi == 0) {
-                        if (!wait_or_abort(bfull(sbb), bph, abort_flag, p.status)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                    }
-                    const uint64_t bd = smem_desc_sw128(b_ring + sbb * p.b_stage_bytes + xi * box_bytes);
+            for (int gg = 0; gg < 4; ++gg) {
+                if (xi == 0) {
+                    ok = __all_sync(0xFFFFFFFFu, wait_or_abort(bfull(sbb), bph, abort_flag, p.status));
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                const uint64_t bd = smem_desc_sw128(b_ring + sbb * p.b_stage_bytes + xi * box_bytes);
+                if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         tc_mma_ts(tmem, a0 + 32 * gg + 8 * kk, bd + 2 * kk, idesc, (sb | gg | kk) != 0);
-                    if (++xi == p.xk || 4 * sb + gg == nchunks - 1) {
-                        tc_commit(bempty(sbb));
-                        xi = 0;
-                        if (++sbb == BS) {
-                            sbb = 0;
-                            bph ^= 1u;
-                        }
+                }
+                __syncwarp();
+                if (++xi == p.xk || 4 * sb + gg == nchunks - 1) {
+                    if (elect_one()) tc_commit(bempty(sbb));
+                    __syncwarp();
+                    xi = 0;
+                    if (++sbb == BS) {
+                        sbb = 0;
+                        bph ^= 1u;
                     }
                 }
-                if (ok) tc_commit(aempty(sa));
-                if (++sa == AS) {
-                    sa = 0;
-                    aph ^= 1u;
-                }
             }
-            tc_commit(accfull);   // also drains in-flight MMAs on the abort path
-            if (!ok) (void)mbar_wait(accfull, 0);
+            if (ok) {
+                if (elect_one()) tc_commit(aempty(sa));
+                __syncwarp();
+            }
+            if (++sa == AS) {
+                sa = 0;
+                aph ^= 1u;
+            }
         }
+        if (elect_one()) tc_commit(accfull);   // also drains in-flight MMAs on the abort path
+        __syncwarp();
+        if (!ok) (void)mbar_wait(accfull, 0);
     }
 
     tc_fence_before();

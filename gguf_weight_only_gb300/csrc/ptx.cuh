@@ -137,6 +137,14 @@ __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+// True in exactly one lane of the converged warp (the lowest active lane).
+__device__ __forceinline__ bool elect_one() {
+    uint32_t p;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\telect.sync _|P, 0xFFFFFFFF;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(p));
+    return p != 0u;
+}
 // Block until the preceding kernel in the stream has completed and its writes are visible.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

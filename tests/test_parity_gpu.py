@@ -168,7 +168,7 @@ def test_deterministic(ql, path, t):
 
 
 @pytest.mark.parametrize("t", TYPES)
-def test_unaligned_source_copied_by_wrapper(ql, t):
+def test_unaligned_source_is_refused_and_a_copy_matches(ql, t):
     """The pages store W at a 68-byte offset (test_llm_quant_cpu.py); the ABI rejects an
     unaligned pointer and an aligned copy gives the oracle's result."""
     N, K, M = 64, 256, 1

@@ -76,8 +76,26 @@ __device__ __forceinline__ uint32_t scale_pair(uint32_t q2, float s, float o) {
     return *reinterpret_cast<const uint32_t *>(&r);
 }
 
+// (q0, q1) fp16 pair of exact integers -> fp16x2(d * q0 + c, d * q1 + c): each product and sum
+// formed exactly by a mixed-precision FMA (f16 inputs, f32 addend and result) and rounded once
+// to fp32, then to fp16.
+__device__ __forceinline__ uint32_t affine_pair(uint32_t q2, uint32_t d2, float c) {
+    float r0, r1;
+    asm("{\n\t.reg .b16 q0, q1, d0, d1;\n\tmov.b32 {q0, q1}, %2;\n\tmov.b32 {d0, d1}, %3;\n\t"
+        "fma.rn.f32.f16 %0, d0, q0, %4;\n\tfma.rn.f32.f16 %1, d0, q1, %4;\n\t}"
+        : "=f"(r0), "=f"(r1)
+        : "r"(q2), "r"(d2), "f"(c));
+    const __half2 r = __floats2half2_rn(r0, r1);
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+
 struct KqRow {
-    float ds[4], ndm[4];   // d*sc and -dmin*m of sub-blocks 2gg + h, gg = 0..3 (exact in fp32)
+    // Sub-blocks 2gg + h, gg = 0..3. The decoded pair v is (1024 + q) (h = 0) or (1024 + 16q)
+    // (h = 1); hfma2(v, sc2, nsc2) with sc2 = sc (sc/16) and nsc2 = -1024 sc (-64 sc) is sc*q,
+    // exact: the fused product is exact and sc*q <= 63*31 fits fp16's 11 bits.
+    uint32_t sc2[4], nsc2[4];
+    float ndm[4];   // -dmin*m (exact in fp32)
+    uint32_t d2;    // (d, d)
 };
 
 __device__ __forceinline__ KqRow kq_row(uint32_t blk, int h) {
@@ -89,11 +107,17 @@ __device__ __forceinline__ KqRow kq_row(uint32_t blk, int h) {
     // pool byte j = value of sub-block j; pick j = h, 2+h, 4+h, 6+h
     const uint32_t sel = static_cast<uint32_t>(h) | ((2u + h) << 4) | ((4u + h) << 8) | ((6u + h) << 12);
     const uint32_t sc4 = prmt(sc_lo4, sc_hi4, sel), m4 = prmt(m_lo4, m_hi4, sel);
-    const float d = half_lo_to_float(hd.x), dmin = half_hi_to_float(hd.x);
+    const float dmin = half_hi_to_float(hd.x);
     KqRow r;
+    r.d2 = prmt(hd.x, 0u, 0x1010u);
+    // scales as exact fp16 pairs (1024 + sc) - 1024, times 1 or 1/16 (exact), and the offsets
+    const uint32_t scale = h ? kH2_1_16 : 0x3C003C00u, off = h ? kH2_m64 : kH2_m1024;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        r.ds[i] = d * static_cast<float>((sc4 >> (8 * i)) & 0xFFu);
+        const uint32_t s = (sc4 >> (8 * i)) & 0xFFu;
+        const uint32_t sc = hsub2((s | (s << 16)) | kH2_1024, kH2_1024);
+        r.sc2[i] = hmul2(sc, scale);
+        r.nsc2[i] = hmul2(sc, off);
         r.ndm[i] = -dmin * static_cast<float>((m4 >> (8 * i)) & 0xFFu);
     }
     return r;
@@ -108,7 +132,8 @@ __device__ __forceinline__ void kq_chunk(uint32_t blk, int gg, const KqRow &r, u
         h0 = lds128(blk + 16);
         h1 = lds128(blk + 32);
     }
-    const float ds = r.ds[gg], ndm = r.ndm[gg];
+    const uint32_t sc2 = r.sc2[gg], nsc2 = r.nsc2[gg], d2 = r.d2;
+    const float ndm = r.ndm[gg];
     const uint32_t j = 2u * gg + h;   // sub-block (and qh bit) of these weights
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
@@ -133,15 +158,10 @@ __device__ __forceinline__ void kq_chunk(uint32_t blk, int gg, const KqRow &r, u
             v01 = or_and(v01, rotl(hq2, rot), mask);
             v23 = or_and(v23, rotl(hq3, rot), mask);
         }
-        if (h == 0) {
-            q01 = hsub2(v01, kH2_1024);
-            q23 = hsub2(v23, kH2_1024);
-        } else {
-            q01 = hfma2(v01, kH2_1_16, kH2_m64);
-            q23 = hfma2(v23, kH2_1_16, kH2_m64);
-        }
-        out[2 * u] = scale_pair(q01, ds, ndm);
-        out[2 * u + 1] = scale_pair(q23, ds, ndm);
+        q01 = hfma2(v01, sc2, nsc2);   // sc*q, exact
+        q23 = hfma2(v23, sc2, nsc2);
+        out[2 * u] = affine_pair(q01, d2, ndm);
+        out[2 * u + 1] = affine_pair(q23, d2, ndm);
     }
 }
 

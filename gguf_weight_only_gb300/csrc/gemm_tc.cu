@@ -309,16 +309,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (threadIdx.x == 0) {
+        // a stage of one superblock is read by the 4 warps of its parity, a wider one by all 8
         for (int s = 0; s < QS; ++s) {
             mbar_init(qfull(s), 1);
-            mbar_init(qempty(s), kDequantWarps);
+            mbar_init(qempty(s), p.S == 1 ? kDequantWarps / 2 : kDequantWarps);
         }
         for (int s = 0; s < BS; ++s) {
             mbar_init(bfull(s), 1);
             mbar_init(bempty(s), 1);
         }
         for (int s = 0; s < kMaxASlots; ++s) {
-            mbar_init(afull(s), kDequantWarps);
+            mbar_init(afull(s), kDequantWarps / 2);   // the 4 warps of one superblock parity
             mbar_init(aempty(s), 1);
         }
         mbar_init(accfull, 1);
@@ -341,22 +342,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp < kDequantWarps) {
         // ---------------------------------------------------- dequantisers
-        const int q = warp & 3, h = warp >> 2;
+        // The two warps of a TMEM lane quarter (one per scheduler pair) take alternate
+        // superblocks and decode both chunk halves of theirs: one warp's hand-off and header
+        // decode then overlap the other's decode, instead of both stalling at the same time.
+        const int q = warp & 3, par = warp >> 2, h = warp >> 2;   // h: epilogue column half
         const int r = 32 * q + lane;
         const int row = min(n0 + r, p.N - 1);
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+        const int lg_s = __ffs(p.S) - 1;   // S is 1, 2 or 4
         bool ok = true;
-        // ring positions as counters (no division on the critical path): weight stage qs with
-        // phase qph and superblock j within it; TMEM A slot sa with phase aph
-        int qs = 0, j = 0, sa = 0;
-        uint32_t qph = 0, aph = 0, stage = 0;
-        for (int sb = 0; sb < p.nsb && ok; ++sb) {
-            if (j == 0) {
-                ok = wait_or_abort(qfull(qs), qph, abort_flag, p.status);
-                ok = __all_sync(0xFFFFFFFFu, ok);
-                if (!ok) break;
-                stage = q_ring + qs * p.q_stage_bytes;
-            }
+        for (int sb = par; sb < p.nsb && ok; sb += 2) {
+            // weight stage sb >> lg_s at ring slot qs with phase qph; its copy may already have
+            // been waited for by this warp (the wait then returns at once: the slot cannot be
+            // refilled before this warp's release of it below)
+            const int si = sb >> lg_s, j = sb & (p.S - 1);
+            const int qs = si % QS;
+            const uint32_t qph = static_cast<uint32_t>(si / QS) & 1u;
+            ok = wait_or_abort(qfull(qs), qph, abort_flag, p.status);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (!ok) break;
+            const uint32_t stage = q_ring + qs * p.q_stage_bytes;
             uint32_t blk = stage + r * p.row_pitch + j * p.bb;
             if constexpr (!TMA)   // block data starts (o & 15) bytes into the row's window (unsigned
                                   // arithmetic wraps modulo 2^32 and keeps the low four bits)
@@ -364,33 +369,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                         static_cast<uint32_t>(p.bb)) & 15u;
             if (!in_bounds(blk + static_cast<uint32_t>(p.bb) <= stage + (r + 1) * p.row_pitch, p.status))
                 blk = stage + r * p.row_pitch;   // bounds check failed: decode the row's first block instead
-            KqRow kr{};
-            if constexpr (TYPE == 12 || TYPE == 13) kr = kq_row(blk, h);
+            KqRow kr0{}, kr1{};
+            if constexpr (TYPE == 12 || TYPE == 13) {
+                kr0 = kq_row(blk, 0);
+                kr1 = kq_row(blk, 1);
+            }
+            const int sa = sb % AS;
+            const uint32_t aph = static_cast<uint32_t>(sb / AS) & 1u;
             ok = wait_or_abort(aempty(sa), aph ^ 1u, abort_flag, p.status);
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t acol = tmem + lane_base + p.a_col + sa * kASlotCols + 16 * h;
-            // the chunk half is warp-uniform: branch once so each decoder is specialised for it
-            if (h == 0) dequant_superblock<TYPE, 0>(blk, kr, acol);
-            else dequant_superblock<TYPE, 1>(blk, kr, acol);
+            const uint32_t acol = tmem + lane_base + p.a_col + sa * kASlotCols;
+            dequant_superblock<TYPE, 0>(blk, kr0, acol);
+            dequant_superblock<TYPE, 1>(blk, kr1, acol + 16);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(afull(sa));
-                if (j == p.S - 1 || sb == p.nsb - 1) mbar_arrive(qempty(qs));
-            }
-            if (++sa == AS) {
-                sa = 0;
-                aph ^= 1u;
-            }
-            if (++j == p.S) {
-                j = 0;
-                if (++qs == QS) {
-                    qs = 0;
-                    qph ^= 1u;
-                }
+                // release the stage after this warp's last superblock in it
+                if ((sb + 2) >> lg_s != si || sb + 2 >= p.nsb) mbar_arrive(qempty(qs));
             }
         }
         // ---------------------------------------------------- epilogue: TMEM -> y

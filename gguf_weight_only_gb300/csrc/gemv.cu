@@ -367,6 +367,44 @@ __device__ __forceinline__ void m1_stage_iq4(uint32_t xtile, uint32_t xexp, int 
     }
 }
 
+// The same records read straight from x in global memory (superblocks at or past nsb as
+// zeros), eight items per lane loaded before any is stored.
+__device__ __forceinline__ void m1_stage_iq4_global(const __half *x, int kb0, int nsb, uint32_t xexp, int kw, int lane) {
+    constexpr int kBatch = 8;
+    const uint32_t nitems = 32u * static_cast<uint32_t>(kw);   // a multiple of 32
+    for (uint32_t q0 = lane; q0 < nitems; q0 += 32u * kBatch) {
+        uint2 vv[kBatch], ww[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const uint32_t q = q0 + 32u * i, b = q >> 5;
+            const uint32_t k = 32u * ((q >> 2) & 7u) + 4u * (q & 3u);
+            vv[i] = ww[i] = make_uint2(0u, 0u);
+            if (q < nitems && kb0 + static_cast<int>(b) < nsb) {
+                const __half *xs = x + static_cast<int64_t>(kb0 + static_cast<int>(b)) * 256 + k;
+                vv[i] = __ldg(reinterpret_cast<const uint2 *>(xs));        // x[k .. k+3]
+                ww[i] = __ldg(reinterpret_cast<const uint2 *>(xs + 16));   // x[k+16 .. k+19]
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const uint32_t q = q0 + 32u * i;
+            if (q >= nitems) break;   // warp-uniform: nitems is a multiple of 32
+            const uint32_t uq = q & 3u, j = (q >> 2) & 7u, b = q >> 5;
+            const uint32_t w4 = uq + 4u * (j & 1u), u = w4 ^ (2u * (j >> 1));
+            const uint2 v = vv[i], w = ww[i];
+            const uint32_t e = xexp + b * kM1Sb + (2u * u) * kM1Rec;
+            sts64(e + 8u * j, prmt(v.x, w.x, 0x5410u), prmt(v.x, w.x, 0x7632u));            // h = 0
+            sts64(e + kM1Rec + 8u * j, prmt(v.y, w.y, 0x5410u), prmt(v.y, w.y, 0x7632u));   // h = 1
+            sts64(e + 8u * (j ^ 1u), 0u, 0u);
+            sts64(e + kM1Rec + 8u * (j ^ 1u), 0u, 0u);
+            if (j < 2u) {
+                sts64(e + 64u, 0u, 0u);
+                sts64(e + kM1Rec + 64u, 0u, 0u);
+            }
+        }
+    }
+}
+
 // One IQ4_XS superblock of rows g, g+8 for the single-token path: acc[0] (row g) and acc[1]
 // (row g+8) gain this lane's sub-blocks 2c, 2c+1. bx_lo / bx_hi = the lane's slot in the
 // superblock's first record for steps 0-3 / 4-7 (the column it carries then, or the zero
@@ -668,11 +706,11 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
             }
             __syncthreads();   // every warp of the CTA runs this set-up
         }
-        // The single-token K-quant records are built straight from x in global memory (no tensor
-        // copy and barrier round trip; measured 1.8-3.6% faster per call). The general kernel's
+        // The single-token records are built straight from x in global memory (no tensor copy and
+        // barrier round trip; measured 1.8-3.6% faster per call for Q4_K). The general kernel's
         // permute pass reading x from global memory instead of the copied tile measured slower
-        // (4096x4096: 4.78 -> 5.21 us), so it keeps the copy, as do IQ4_XS and the prologues.
-        constexpr bool M1_DIRECT = M1 && !PRO && TYPE != 23;
+        // (4096x4096: 4.78 -> 5.21 us), so it keeps the copy, as do the fused prologues.
+        constexpr bool M1_DIRECT = M1 && !PRO;
         if constexpr (!PRO && !M1_DIRECT) {
             if (nmine > 0 && lane == 0) {   // this warp's x slice, all tokens, once
                 mbar_arrive_expect_tx(xbar, p.x_tx);
@@ -758,10 +796,16 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
             __syncwarp();
         }
         if constexpr (M1) {   // after the tile is complete (copied, or filled by a prologue)
-            if constexpr (TYPE == 23) m1_stage_iq4(xreg, xexp, p.kw, lane);
-            else if constexpr (M1_DIRECT) {
-                if (nmine > 0) m1_stage_global(p.x, kb0, p.nsb, xexp, xsums, p.kw, lane, p.qswap);
-            } else m1_stage(xreg, xexp, xsums, p.kw, lane, p.qswap);
+            if constexpr (M1_DIRECT) {
+                if (nmine > 0) {
+                    if constexpr (TYPE == 23) m1_stage_iq4_global(p.x, kb0, p.nsb, xexp, p.kw, lane);
+                    else m1_stage_global(p.x, kb0, p.nsb, xexp, xsums, p.kw, lane, p.qswap);
+                }
+            } else if constexpr (TYPE == 23) {
+                m1_stage_iq4(xreg, xexp, p.kw, lane);
+            } else {
+                m1_stage(xreg, xexp, xsums, p.kw, lane, p.qswap);
+            }
             __syncwarp();
         }
     } else {

@@ -145,20 +145,21 @@ struct GemvMaps {
 
 constexpr uint32_t kM1Rec = 72, kM1Sb = 16 * kM1Rec;   // record and superblock strides of the staged B
 
-// Builds the staged B records and the sub-block sums from the warp's x tile (M = 1: row
-// r = 4 b + segment of 128 bytes, chunk p of row r stored at p ^ (r & 7)).
-__device__ __forceinline__ void m1_stage(uint32_t xtile, uint32_t xexp, uint32_t xsums, int kw, int lane, int qswap) {
-    const uint32_t nitems = 64u * static_cast<uint32_t>(kw);   // (superblock, sub-block, word): a multiple of 32
-    for (uint32_t q = lane; q < nitems; q += 32) {
-        const uint32_t u = q & 7u, j = (q >> 3) & 7u, b = q >> 6;
-        const uint32_t k = 32u * j + 4u * u;          // position in the superblock
-        const uint32_t r = 4u * b + (k >> 6), col = k & 63u;
-        const uint2 v = lds64(xtile + r * 128u + ((((col >> 3) ^ (r & 7u))) << 4) + ((col & 4u) << 1));
-        const uint32_t p02 = prmt(v.x, v.y, 0x5410u), p13 = prmt(v.x, v.y, 0x7632u);   // (x0, x2), (x1, x3)
-        // records 2u and 2u+1, slot j (the records of word u ^ 4 when the column's carrier reads
-        // its quant halves swapped)
+// Chunk `lane` (x[8 lane .. 8 lane + 7]) of superblock b of the slice, already in registers, laid
+// out as the plain staging lays out its items 2 (lane & 3) and 2 (lane & 3) + 1 of sub-block
+// lane >> 2. The sub-block sum is formed in the plain staging's order: each item's pair sums,
+// then the item pair (in lane), then shuffles across the sub-block's four lanes (fp32 addition
+// is commutative, so every lane of a pair holds the same sum at each step).
+__device__ __forceinline__ void m1_stage_chunk(const uint4 &v, int b, uint32_t xexp, uint32_t xsums, int lane, int qswap) {
+    const uint32_t j = static_cast<uint32_t>(lane) >> 2, m = static_cast<uint32_t>(lane) & 3u;
+    float s2[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t vx = h ? v.z : v.x, vy = h ? v.w : v.y;
+        const uint32_t u = 2u * m + static_cast<uint32_t>(h);
+        const uint32_t p02 = prmt(vx, vy, 0x5410u), p13 = prmt(vx, vy, 0x7632u);
         const uint32_t us = u ^ ((qswap && ((j >> 1) & 1u)) ? 4u : 0u);
-        const uint32_t e = xexp + b * kM1Sb + (2u * us) * kM1Rec + 8u * j;
+        const uint32_t e = xexp + static_cast<uint32_t>(b) * kM1Sb + (2u * us) * kM1Rec + 8u * j;
         if (j & 1u) {
             sts64(e, 0u, p02);
             sts64(e + kM1Rec, 0u, p13);
@@ -166,25 +167,49 @@ __device__ __forceinline__ void m1_stage(uint32_t xtile, uint32_t xexp, uint32_t
             sts64(e, p02, 0u);
             sts64(e + kM1Rec, p13, 0u);
         }
-        if (j == 0u) {   // the zero slots of records 2u, 2u+1 (column 0 is never swapped)
+        if (j == 0u) {
             sts64(e + 64u, 0u, 0u);
             sts64(e + kM1Rec + 64u, 0u, 0u);
         }
-        const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
-        const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
-        float sum = (f0.x + f0.y) + (f1.x + f1.y);
-        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);   // the eight words of one sub-block sit in
-        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);   // eight neighbouring lanes
-        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
-        if (u == 0u) sts32(xsums + (b * 8u + j) * 4u, __float_as_uint(sum));
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&vx));
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&vy));
+        s2[h] = (f0.x + f0.y) + (f1.x + f1.y);
+    }
+    float sum = s2[0] + s2[1];
+    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+    if (m == 0u) sts32(xsums + (static_cast<uint32_t>(b) * 8u + j) * 4u, __float_as_uint(sum));
+}
+
+// IQ4_XS: the lanes holding the first half of a sub-block (lane & 3 < 2) lay out their two items
+// with the x[k+16 ..] words taken from the lane two above.
+__device__ __forceinline__ void m1_stage_iq4_chunk(const uint4 &v, int b, uint32_t xexp, int lane) {
+    const uint4 w = make_uint4(__shfl_xor_sync(0xFFFFFFFFu, v.x, 2), __shfl_xor_sync(0xFFFFFFFFu, v.y, 2),
+                               __shfl_xor_sync(0xFFFFFFFFu, v.z, 2), __shfl_xor_sync(0xFFFFFFFFu, v.w, 2));
+    const uint32_t j = static_cast<uint32_t>(lane) >> 2, m = static_cast<uint32_t>(lane) & 3u;
+    if (m >= 2u) return;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t uq = 2u * m + static_cast<uint32_t>(h);
+        const uint32_t vx = h ? v.z : v.x, vy = h ? v.w : v.y, wx = h ? w.z : w.x, wy = h ? w.w : w.y;
+        const uint32_t w4 = uq + 4u * (j & 1u), u = w4 ^ (2u * (j >> 1));
+        const uint32_t e = xexp + static_cast<uint32_t>(b) * kM1Sb + (2u * u) * kM1Rec;
+        sts64(e + 8u * j, prmt(vx, wx, 0x5410u), prmt(vx, wx, 0x7632u));            // h = 0
+        sts64(e + kM1Rec + 8u * j, prmt(vy, wy, 0x5410u), prmt(vy, wy, 0x7632u));   // h = 1
+        sts64(e + 8u * (j ^ 1u), 0u, 0u);
+        sts64(e + kM1Rec + 8u * (j ^ 1u), 0u, 0u);
+        if (j < 2u) {
+            sts64(e + 64u, 0u, 0u);
+            sts64(e + kM1Rec + 64u, 0u, 0u);
+        }
     }
 }
 
-// The same records and sums read straight from x in global memory: superblocks [kb0, kb0 + kw)
-// of the warp's slice, those at or past nsb as zeros. Item q of a superblock is x[4q .. 4q+3],
-// so a warp's 32 items are 256 contiguous bytes; eight items per lane are loaded before any is
-// used. Used where x is plain input (no fused prologue fills a tile first): it saves the tensor
-// copy's round trip through the barrier and the shared-memory tile.
+// Builds the staged B records and the fp32 sub-block sums straight from x in global memory:
+// superblocks [kb0, kb0 + kw) of the warp's slice, those at or past nsb as zeros. Item q
+// (sub-block j = q >> 3 & 7, word u = q & 7) of a superblock is x[4q .. 4q+3], so a warp's 32
+// items are 256 contiguous bytes; eight items per lane are loaded before any is used. Reading x
+// directly saves a tensor copy's round trip through a barrier and a shared-memory tile.
 __device__ __forceinline__ void m1_stage_global(const __half *x, int kb0, int nsb, uint32_t xexp, uint32_t xsums,
                                                 int kw, int lane, int qswap) {
     constexpr int kBatch = 8;
@@ -341,34 +366,11 @@ __device__ __forceinline__ void iq4_lut_fill(uint32_t lut) {
     }
 }
 
-// The staged B records of the IQ4_XS single-token path from the warp's x tile (M = 1, row
-// r = 4 b + segment, chunk p of row r stored at p ^ (r & 7)); item (b, j, word w & 3) writes
-// slot j of records 2u, 2u+1 (u = w ^ 2 (j >> 1), the step at which its carrier holds word w)
-// and zeros slot j ^ 1 of both (and slot 8 when j < 2).
-__device__ __forceinline__ void m1_stage_iq4(uint32_t xtile, uint32_t xexp, int kw, int lane) {
-    const uint32_t nitems = 32u * static_cast<uint32_t>(kw);   // a multiple of 32
-    auto x4 = [&](uint32_t b, uint32_t k) {   // x[k .. k+3] of superblock b (k % 4 == 0)
-        const uint32_t r = 4u * b + (k >> 6), col = k & 63u;
-        return lds64(xtile + r * 128u + ((((col >> 3) ^ (r & 7u))) << 4) + ((col & 4u) << 1));
-    };
-    for (uint32_t q = lane; q < nitems; q += 32) {
-        const uint32_t uq = q & 3u, j = (q >> 2) & 7u, b = q >> 5;
-        const uint32_t w4 = uq + 4u * (j & 1u), u = w4 ^ (2u * (j >> 1)), k = 32u * j + 4u * uq;
-        const uint2 v = x4(b, k), w = x4(b, k + 16u);   // x[k..k+3], x[k+16..k+19]
-        const uint32_t e = xexp + b * kM1Sb + (2u * u) * kM1Rec;
-        sts64(e + 8u * j, prmt(v.x, w.x, 0x5410u), prmt(v.x, w.x, 0x7632u));                   // h = 0
-        sts64(e + kM1Rec + 8u * j, prmt(v.y, w.y, 0x5410u), prmt(v.y, w.y, 0x7632u));          // h = 1
-        sts64(e + 8u * (j ^ 1u), 0u, 0u);
-        sts64(e + kM1Rec + 8u * (j ^ 1u), 0u, 0u);
-        if (j < 2u) {
-            sts64(e + 64u, 0u, 0u);
-            sts64(e + kM1Rec + 64u, 0u, 0u);
-        }
-    }
-}
-
-// The same records read straight from x in global memory (superblocks at or past nsb as
-// zeros), eight items per lane loaded before any is stored.
+// The staged B records of the IQ4_XS single-token path, read straight from x in global memory
+// (superblocks at or past nsb as zeros; eight items per lane loaded before any is stored). Item
+// (b, j, word w & 3) writes slot j of records 2u, 2u+1 (u = w ^ 2 (j >> 1), the step at which
+// its carrier holds word w) and zeros slot j ^ 1 of them; the zero slot 8 is written by the
+// items of sub-blocks 0 and 1.
 __device__ __forceinline__ void m1_stage_iq4_global(const __half *x, int kb0, int nsb, uint32_t xexp, int kw, int lane) {
     constexpr int kBatch = 8;
     const uint32_t nitems = 32u * static_cast<uint32_t>(kw);   // a multiple of 32
@@ -550,7 +552,7 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
     const uint32_t xreg = base + p.x_offset + warp * p.x_warp_bytes;
     const uint32_t xsum_base = xreg + p.x_tx;   // XSUM: [token][superblock of the slice] x 32 bytes
     // M1: staged B records [superblock][16 MMAs][9 slots] x 8 bytes, then fp32 sums [superblock][8]
-    const uint32_t xexp = xreg + p.x_tx, xsums = xexp + kM1Sb * p.kw;
+    const uint32_t xexp = xreg, xsums = xexp + kM1Sb * p.kw;   // (no x tile in the single-token kernels)
     const uint32_t ring = base + p.ring_offset + warp * D * p.slot_bytes;
 
     const uint32_t ring_end = base + p.ring_offset + (blockDim.x >> 5) * D * p.slot_bytes;
@@ -559,7 +561,9 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
         asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
         const bool lay = ring_end - smem_u32(smem) <= dyn && p.red_offset >= scratch_offset(blockDim.x >> 5, D) &&
                          p.x_offset >= p.red_offset && p.ring_offset >= p.x_offset + (blockDim.x >> 5) * p.x_warp_bytes &&
-                         (!XRES || p.x_tx <= p.x_warp_bytes) && p.w_bytes + (XRES ? 0u : p.x_bytes) <= p.slot_bytes &&
+                         (!XRES || (M1 ? kM1Sb * p.kw + (TYPE == 23 ? 0u : 32u * p.kw) <= p.x_warp_bytes
+                                       : p.x_tx <= p.x_warp_bytes)) &&
+                         p.w_bytes + (XRES ? 0u : p.x_bytes) <= p.slot_bytes &&
                          (!(M1 && TYPE == 23) || (p.lut_offset >= p.red_offset && p.lut_offset + kIq4LutBytes <= p.x_offset));
         if (!in_bounds(lay, p.status)) return;
     }
@@ -718,7 +722,7 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
             }
             if (nmine > 0) ok = mbar_wait(xbar, 0);
         }
-        if constexpr (PERM || PRO) {
+        if constexpr ((PERM || PRO) && !M1) {
             // One pass over the warp's x tile: fill it (fused prologue), permute it in place
             // [x0 x1 x2 x3] -> [x0 x2 x1 x3] inside every 16-byte chunk (K-quants, Q6_K) and,
             // for the K-quants, store the sums of x over each 32-wide sub-block. The tile is
@@ -795,16 +799,43 @@ __global__ void __launch_bounds__(32 * GemvFmt<TYPE>::MAXW, 1) gemv_kernel(const
             }
             __syncwarp();
         }
-        if constexpr (M1) {   // after the tile is complete (copied, or filled by a prologue)
+        if constexpr (M1) {   // the staged B records, built without an x tile
             if constexpr (M1_DIRECT) {
                 if (nmine > 0) {
                     if constexpr (TYPE == 23) m1_stage_iq4_global(p.x, kb0, p.nsb, xexp, p.kw, lane);
                     else m1_stage_global(p.x, kb0, p.nsb, xexp, xsums, p.kw, lane, p.qswap);
                 }
-            } else if constexpr (TYPE == 23) {
-                m1_stage_iq4(xreg, xexp, p.kw, lane);
-            } else {
-                m1_stage(xreg, xexp, xsums, p.kw, lane, p.qswap);
+            } else if (nmine > 0) {
+                // fused prologue: lane l computes the 8 activations of chunk l of each superblock
+                // (loads of kFillGroup superblocks issued first) and lays them out as the plain
+                // staging does, with the sub-block sums added in the same order
+                float rstd = 0.f;
+                if (p.pro == 2) {
+                    float tot = 0.f;
+                    for (int w2 = 0; w2 < static_cast<int>(blockDim.x >> 5); ++w2) tot += sq[w2 * kGemvMaxM];
+                    rstd = rsqrtf(tot / static_cast<float>(p.K) + p.eps);
+                }
+                for (int b0 = 0; b0 < p.kw; b0 += kFillGroup) {
+                    ChunkIn in[kFillGroup];
+#pragma unroll
+                    for (int i = 0; i < kFillGroup; ++i) {
+                        const int64_t k0 = static_cast<int64_t>(kb0 + b0 + i) * 256 + 8 * lane;
+                        if (b0 + i < p.kw && k0 < p.K) in[i] = chunk_load(p, 0, k0);
+                    }
+#pragma unroll
+                    for (int i = 0; i < kFillGroup; ++i) {
+                        if (b0 + i >= p.kw) break;   // warp-uniform
+                        const int64_t k0 = static_cast<int64_t>(kb0 + b0 + i) * 256 + 8 * lane;
+                        uint4 v = make_uint4(0u, 0u, 0u, 0u);   // superblocks past nsb
+                        if (k0 < p.K) {
+                            v = chunk_compute(p, in[i], rstd);
+                            if (p.pro == 2 && p.xnorm && b == 0 && tg == 0)   // one writer per element
+                                *reinterpret_cast<uint4 *>(p.xnorm + k0) = v;
+                        }
+                        if constexpr (TYPE == 23) m1_stage_iq4_chunk(v, b0 + i, xexp, lane);
+                        else m1_stage_chunk(v, b0 + i, xexp, xsums, lane, p.qswap);
+                    }
+                }
             }
             __syncwarp();
         }
@@ -1042,7 +1073,8 @@ GemvPlan make_plan(int type, int64_t T, int64_t K, int M, int num_sms, bool need
         o.x_bytes = xres ? 0u : o.x_tx;
         const uint32_t xsum_bytes = (type == 12 || type == 13) ? static_cast<uint32_t>(M * kw * 32) : 0u;
         const uint32_t m1_bytes = m1 ? static_cast<uint32_t>(kw * (16 * 72) + (type == 23 ? 0 : kw * 32)) : 0u;
-        o.x_warp_bytes = xres ? ((o.x_tx + (m1 ? m1_bytes : xsum_bytes) + 1023u) & ~1023u) : 0u;
+        // the single-token kernels build their records without an x tile
+        o.x_warp_bytes = xres ? (((m1 ? 0u : o.x_tx) + (m1 ? m1_bytes : xsum_bytes) + 1023u) & ~1023u) : 0u;
         // a slot that also holds a 128-byte-swizzled x tile starts on 1 KB, weights alone on 128 B
         o.slot_bytes = xres ? ((o.w_bytes + 127u) & ~127u) : ((o.x_bytes + o.w_bytes + 1023u) & ~1023u);
         o.xres = xres ? 1 : 0;

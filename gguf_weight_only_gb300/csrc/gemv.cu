@@ -1218,14 +1218,15 @@ cudaError_t launch_impl(int type, int nproj, const GemvProj *proj, const __half 
         if (T > (int64_t(1) << 30)) return cudaErrorInvalidValue;
     }
     tile0[nproj] = static_cast<int>(T);
-    // One token, K-quants: the single-token kernel when its larger x region fits and each warp
-    // has at least 8 superblocks to decode (its once-per-launch staging of x costs more than it
-    // saves on fewer: measured slower on K=4096 N=4096). The choice depends on the shape only,
-    // so a prologue or the greedy head sums exactly as the plain call does.
+    // One token: the single-token kernel when its plan fits and each warp has at least 2
+    // superblocks to decode. With its x staged straight from global memory it measured 1-2.5%
+    // faster than the general kernel on K=4096 N=4096 and N=1024 and 2% slower on K=1024
+    // N=1024 (one superblock per warp). The choice depends on the shape only, so a prologue or
+    // the greedy head sums exactly as the plain call does.
     const int64_t grid = std::min<int64_t>(num_sms > 0 ? num_sms : 1, T);
     const int64_t per_warp = (T + grid - 1) / grid * ((K / 256 + 7) / 8);   // tiles per CTA x superblocks per slice of 8
     const bool m1_type = type == 12 || type == 13 || (type == 23 && (K / 256) % 2 == 0 && !iq4_single_token_off());
-    bool m1 = M == 1 && m1_type && per_warp >= 8 && !single_token_off();
+    bool m1 = M == 1 && m1_type && per_warp >= 2 && !single_token_off();
     GemvPlan pl = make_plan(type, T, K, M, num_sms, pro != 0 || head, m1);
     if (m1 && pl.smem > 227 * 1024) {
         m1 = false;

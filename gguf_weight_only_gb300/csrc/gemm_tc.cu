@@ -4,23 +4,24 @@
 // Tiling ("swap AB"): a CTA owns 128 weight rows (the MMA's M side, one TMEM lane per row)
 // and a tile of n_tile tokens (the MMA's N side, 32..256). The fp32 accumulator lives in
 // TMEM columns [0, n_tile). K is walked superblock by superblock (256 k = 16 MMAs of K = 16);
-// every hand-off between roles is per superblock, because on this part the issuing thread's
-// fixed cost per wait/fence/commit round (several hundred cycles) is far above the cost of
-// one MMA issue (about 50 cycles) and would otherwise starve the tensor pipe at small N.
+// every hand-off between roles is per superblock, because a wait/fence/commit round costs
+// several hundred cycles, far above one MMA issue (about 30 cycles at small N), and finer
+// hand-offs would starve the tensor pipe at small N.
 //
 // Warp roles (352 threads):
 //   warps 0-7  dequantisers: warp w serves TMEM lane quarter w % 4 (rows 32(w%4)..+31, one
-//              thread per row) and half w / 4 of every 64-wide chunk. Each thread decodes its
-//              row's 4 x 32 weights of a superblock from the staged block into fp16 and writes
+//              thread per row) and the superblocks of parity w / 4. Each thread decodes its
+//              row's 256 weights of a superblock from the staged block into fp16 and writes
 //              them with tcgen05.st into a TMEM A-operand ring (2 or 3 superblock slots of 128
 //              columns); the MMA reads A straight from TMEM, so dequantised weights never touch
-//              shared memory. After the K loop the same warps drain the accumulator to y.
+//              shared memory. After the K loop the same warps drain the accumulator to y, warp
+//              w taking the column half w / 4.
 //   warp 8     weight producer: one 2-D TMA tensor copy per stage (S superblocks of the 128
 //              rows) into a shared-memory ring when rows are 16-byte multiples, else one bulk
 //              copy per row over the aligned window around the row's span.
 //   warp 9     activation producer: 2-D TMA of the x tile [n_tile tokens x 64 k], 128-byte
 //              swizzled, the MMA's B operand.
-//   warp 10    TMEM allocator and the single MMA-issuing thread.
+//   warp 10    TMEM allocator and MMA issue (the warp runs the loop, one elected lane issues).
 // All hand-offs are mbarriers; every wait is bounded and an expired wait aborts the CTA
 // (status word set, TMEM freed).
 #include <algorithm>
@@ -65,9 +66,10 @@ struct GemmArgs {
 // ------------------------------------------------------------ per-row dequantisers
 // Each produces the 32 fp16 weights k = 32h .. 32h+31 of 64-wide chunk gg of one row as 16
 // packed pairs (k, k+1), i.e. the 16 TMEM columns [16h, 16h+16) of that chunk. Every weight is
-// formed in fp32 from exact parts (the integer code as an exact fp16 pair, the scale products
-// d*sc and dmin*m exact in fp32) and rounded to fp16 once: the MMA operand is the weight to
-// within one fp16 rounding, also where d*sc*q and dmin*m nearly cancel.
+// formed exactly and rounded to fp16 once (K-quants: d * (sc q) - dmin m by one mixed-precision
+// FMA with sc q an exact fp16 integer; Q6_K and IQ4_XS: the integer code times the fp32 scale),
+// so the MMA operand is the weight to within one fp16 rounding, also where d sc q and dmin m
+// nearly cancel.
 
 // (q0, q1) exact integers in fp16 -> fp16x2(q0 * s + o, q1 * s + o), each rounded once
 __device__ __forceinline__ uint32_t scale_pair(uint32_t q2, float s, float o) {

@@ -65,11 +65,12 @@ struct GemmArgs {
 
 // ------------------------------------------------------------ per-row dequantisers
 // Each produces the 32 fp16 weights k = 32h .. 32h+31 of 64-wide chunk gg of one row as 16
-// packed pairs (k, k+1), i.e. the 16 TMEM columns [16h, 16h+16) of that chunk. Every weight is
-// formed exactly and rounded to fp16 once (K-quants: d * (sc q) - dmin m by one mixed-precision
-// FMA with sc q an exact fp16 integer; Q6_K and IQ4_XS: the integer code times the fp32 scale),
-// so the MMA operand is the weight to within one fp16 rounding, also where d sc q and dmin m
-// nearly cancel.
+// packed pairs (k, k+1), i.e. the 16 TMEM columns [16h, 16h+16) of that chunk. K-quant weights
+// d * (sc q) - dmin m are formed by one mixed-precision FMA (sc q an exact fp16 integer) and
+// rounded once to fp32 and once to fp16, so the MMA operand is the weight to within one fp16
+// rounding also where d sc q and dmin m nearly cancel. Q6_K and IQ4_XS weights are the integer
+// code times the fp32 scale (d sc exact), whose product may round in fp32 (at most 2^-24
+// relative) before the fp16 rounding.
 
 // (q0, q1) exact integers in fp16 -> fp16x2(q0 * s + o, q1 * s + o), each rounded once
 __device__ __forceinline__ uint32_t scale_pair(uint32_t q2, float s, float o) {

@@ -21,10 +21,12 @@
 //    sub-block sums.
 //  * Per-tile partials of the warps go to shared memory; after a round of tiles they are
 //    summed over the K slices in fixed order (deterministic).
-//  * One token with K-quants (when each warp has at least 8 superblocks) takes a specialised
-//    kernel that puts the eight sub-blocks on the MMA's n side instead of tokens, feeds the
-//    quants as exact fp16 subnormals and applies scales once per sub-block in fp32 (see the
-//    single-token section below). QL_GEMV_M1=0 in the environment disables it (A/B timing).
+//  * One token with K-quants or IQ4_XS (when each warp has at least 2 superblocks) takes a
+//    specialised kernel that puts the eight sub-blocks on the MMA's n side instead of tokens,
+//    feeds the quants as exact fp16 subnormals (IQ4_XS: codebook pairs from a byte table),
+//    applies scales once per sub-block in fp32, and stages its x records straight from global
+//    memory, without an x tile (see the single-token sections below). QL_GEMV_M1=0 in the
+//    environment disables it (A/B timing).
 //  * Variants of the launch (several projections; a fused prologue; the greedy-head epilogue)
 //    are separate instantiations, so the plain kernel compiles as if they did not exist.
 // Fragment ownership and the per-format decoders: decode.cuh.

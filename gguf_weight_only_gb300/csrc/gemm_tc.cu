@@ -24,10 +24,17 @@
 //   warp 10    TMEM allocator and MMA issue (the warp runs the loop, one elected lane issues).
 // All hand-offs are mbarriers; every wait is bounded and an expired wait aborts the CTA
 // (status word set, TMEM freed).
+//
+// Few row tiles (at most half the SM count) and M <= 256 take gemm_split_kernel instead: all M
+// tokens in one tile and each row tile's superblocks shared by a pair of CTAs in a thread-block
+// cluster, the second adding its partial sums into the first's through one bulk copy between
+// their shared memories. Several token tiles would each decode every weight again.
 #include <algorithm>
 #include <climits>
 #include <cstdint>
 #include <cuda.h>
+#include <mutex>
+#include <vector>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -43,6 +50,11 @@ constexpr uint32_t kASlotCols = 128;
 constexpr int kDequantWarps = 8;
 constexpr int kThreads = 32 * 11;
 constexpr uint32_t kTmemCols = 512;
+constexpr int kAccBars = 2;         // accumulator final; (head) the tail's partial sums handed over
+// Heads per tail in the split kernel. Measured on GB300 (M=32, K=4096, N=12288, where pairs
+// would need 192 CTAs): three heads per tail gave Q4_K 18.8 -> 19.4 us, Q5_K 20.6 -> 20.1,
+// Q6_K 39.9 -> 38.3, IQ4_XS 25.9 -> 22.1; pairs gain 1.75-1.9x wherever they fit.
+constexpr int kMaxSplitK = 1;
 
 struct GemmArgs {
     const uint8_t *W;
@@ -61,6 +73,14 @@ struct GemmArgs {
     int64_t total_bytes;
     int bb;                    // bytes per superblock
     int type;
+    // Work split (the SPLIT kernel, one token tile): clusters of k + 1 CTAs. Rank r < k is the head of
+    // row tile cid k + r and takes superblocks [0, L); rank k takes the tails [L, nsb) of the
+    // cluster's tiles back to back, tile i's sums in TMEM columns [i n_tile, (i+1) n_tile). The
+    // tail stages tile i's sums at the base of its shared memory (rows of part_stride floats)
+    // and copies them into head i's receive area at recv_off.
+    // Unsplit: one CTA per (row tile, token tile), all superblocks.
+    int k, L, tail, row_tiles, part_stride;
+    uint32_t recv_off;
 };
 
 // ------------------------------------------------------------ per-row dequantisers
@@ -575,6 +595,382 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// Split form for one token tile over few row tiles: clusters of k + 1 CTAs, where rank r < k
+// (a head) takes superblocks [0, L) of row tile cid k + r and rank k (the tail) the remaining
+// [L, nsb) of all k tiles, tile after tile, with tile i's sums in TMEM columns [i n_tile,
+// (i+1) n_tile). The roles and hand-offs inside a CTA are those of gemm_kernel; the superblock
+// position v of a CTA maps to (row tile, superblock) through counters stepped with v. At the end
+// the tail stages each tile's sums in its idle rings and copies them with one bulk
+// shared-to-shared copy into that head's receive area, completing on the head's barrier pfull;
+// the head adds them after its own (a fixed order, so results are reproducible) and stores y.
+// A separate kernel rather than a branch of gemm_kernel: folded into it, the unsplit path ran
+// 2% slower (Q4_K M=512, GB300).
+template <int TYPE, bool TMA>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_split_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap, const GemmArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *const gbase = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const uint32_t b_ring = base;
+    const uint32_t q_ring = base + p.q_off;
+    const uint32_t bars = base + p.bar_off;
+    const int QS = p.qstages, BS = p.bstages;
+    auto qfull = [&](int s) { return bars + 8u * s; };
+    auto qempty = [&](int s) { return bars + 8u * (QS + s); };
+    auto bfull = [&](int s) { return bars + 8u * (2 * QS + s); };
+    auto bempty = [&](int s) { return bars + 8u * (2 * QS + BS + s); };
+    auto afull = [&](int s) { return bars + 8u * (2 * QS + 2 * BS + s); };
+    auto aempty = [&](int s) { return bars + 8u * (2 * QS + 2 * BS + kMaxASlots + s); };
+    const uint32_t accfull = bars + 8u * (2 * QS + 2 * BS + 2 * kMaxASlots);
+    const uint32_t pfull = accfull + 8u;   // head: the tail's partial sums have landed in the receive area
+    const uint32_t misc_off = p.bar_off + 8u * (2 * QS + 2 * BS + 2 * kMaxASlots + kAccBars);
+    const int AS = p.a_slots;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + misc_off);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + misc_off + 4);
+
+    const int crank = static_cast<int>(cluster_rank());
+    const bool is_tail = crank == p.k;
+    const int tile_c = static_cast<int>(blockIdx.x) / (p.k + 1) * p.k;   // the cluster's first row tile
+    const int kk = min(p.k, p.row_tiles - tile_c);                        // row tiles of this cluster
+    const int nv = is_tail ? kk * p.tail : (crank < kk ? p.L : 0);        // superblock positions of this CTA
+    const int own_tile = tile_c + crank;
+    const uint32_t part_bytes = static_cast<uint32_t>(kRows * p.part_stride) * 4u;   // one tile's sums
+    // (row tile, superblock) of position v: the superblock advances by one and, in the tail,
+    // wraps from nsb to L with the next tile (counters: a division per superblock would cost the
+    // issuing warps more than its MMAs)
+    const int tile0 = is_tail ? tile_c : own_tile, sb0 = is_tail ? p.L : 0;
+    auto step = [&](int &tile, int &sb, int by) {
+        sb += by;
+        while (is_tail && sb >= p.nsb) {
+            sb -= p.tail;
+            ++tile;
+        }
+    };
+    const int nchunks = nv * 4;
+    if constexpr (kBoundsChecks) {   // rings, barriers, hand-off areas and TMEM columns inside their budgets
+        uint32_t dyn;
+        asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+        const uint32_t q_end = p.q_off + static_cast<uint32_t>(QS) * p.q_stage_bytes;
+        const bool lay = misc_off + 8u + (base - raw) <= dyn && static_cast<uint32_t>(BS) * p.b_stage_bytes <= p.q_off &&
+                         q_end <= p.recv_off && p.recv_off + part_bytes <= p.bar_off &&
+                         static_cast<uint32_t>(p.k) * part_bytes <= q_end &&
+                         p.q_stage_bytes >= kRows * p.row_pitch && p.row_pitch >= static_cast<uint32_t>(p.S * p.bb) &&
+                         static_cast<uint32_t>(p.n_tile * p.k) <= p.a_col && AS <= kMaxASlots &&
+                         p.a_col + static_cast<uint32_t>(AS) * kASlotCols <= kTmemCols &&
+                         p.b_stage_bytes >= static_cast<uint32_t>(p.xk * p.n_tile) * 128u && p.M <= p.n_tile;
+        if (!in_bounds(lay, p.status)) return;
+    }
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < QS; ++s) {
+            mbar_init(qfull(s), 1);
+            mbar_init(qempty(s), p.S == 1 ? kDequantWarps / 2 : kDequantWarps);
+        }
+        for (int s = 0; s < BS; ++s) {
+            mbar_init(bfull(s), 1);
+            mbar_init(bempty(s), 1);
+        }
+        for (int s = 0; s < kMaxASlots; ++s) {
+            mbar_init(afull(s), kDequantWarps / 2);
+            mbar_init(aempty(s), 1);
+        }
+        mbar_init(accfull, 1);
+        mbar_init(pfull, 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+        if (!is_tail && crank < kk) mbar_arrive_expect_tx(pfull, part_bytes);   // the one arrival; the copy brings the bytes
+    }
+    if (warp == 10) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 9 && lane == 0) prefetch_tmap(&xmap);
+    if (TMA && warp == 8 && lane == 0) prefetch_tmap(&wmap);
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();   // every barrier of the cluster is initialised before any copy reaches it
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_launch_dependents();
+
+    if (warp < kDequantWarps) {
+        // ---------------------------------------------------- dequantisers (as in gemm_kernel)
+        const int q = warp & 3, par = warp >> 2, h = warp >> 2;
+        const int r = 32 * q + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+        const int lg_s = __ffs(p.S) - 1;
+        bool ok = true;
+        for (int v = par; v < nv && ok; v += 2) {
+            // (row tile, superblock) of position v: one division per superblock of decode work
+            const int sb = is_tail ? p.L + v % p.tail : v;
+            const int row = min((is_tail ? tile_c + v / p.tail : own_tile) * kRows + r, p.N - 1);
+            // a stage never spans two row tiles (L and tail are multiples of S)
+            const int si = v >> lg_s, j = v & (p.S - 1);
+            const int qs = si % QS;
+            const uint32_t qph = static_cast<uint32_t>(si / QS) & 1u;
+            ok = __all_sync(0xFFFFFFFFu, wait_or_abort(qfull(qs), qph, abort_flag, p.status));
+            if (!ok) break;
+            const uint32_t stage = q_ring + qs * p.q_stage_bytes;
+            uint32_t blk = stage + r * p.row_pitch + j * p.bb;
+            if constexpr (!TMA)
+                blk += ((static_cast<uint32_t>(row) * static_cast<uint32_t>(p.nsb) + static_cast<uint32_t>(sb - j)) *
+                        static_cast<uint32_t>(p.bb)) & 15u;
+            if (!in_bounds(blk + static_cast<uint32_t>(p.bb) <= stage + (r + 1) * p.row_pitch, p.status))
+                blk = stage + r * p.row_pitch;
+            KqRow kr0{}, kr1{};
+            if constexpr (TYPE == 12 || TYPE == 13) {
+                kr0 = kq_row(blk, 0);
+                kr1 = kq_row(blk, 1);
+            }
+            const int sa = v % AS;
+            const uint32_t aph = static_cast<uint32_t>(v / AS) & 1u;
+            ok = __all_sync(0xFFFFFFFFu, wait_or_abort(aempty(sa), aph ^ 1u, abort_flag, p.status));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t acol = tmem + lane_base + p.a_col + sa * kASlotCols;
+            dequant_superblock<TYPE, 0>(blk, kr0, acol);
+            dequant_superblock<TYPE, 1>(blk, kr1, acol + 16);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(afull(sa));
+                if ((v + 2) >> lg_s != si || v + 2 >= nv) mbar_arrive(qempty(qs));
+            }
+        }
+        // ---------------------------------------------------- epilogue
+        if (ok) ok = wait_or_abort(accfull, 0, abort_flag, p.status);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        const int ng = p.n_tile / 16, g_mid = ng / 2;
+        const int c_lo = 16 * (h ? g_mid : 0), c_hi = 16 * (h ? ng : g_mid);
+        if (is_tail) {
+            // tile i's sums to rows [i 128, (i+1) 128) of the staging area at the base of shared
+            // memory (the rings are idle once the accumulators are final), then one bulk copy per
+            // head; sent even after an abort (the heads then see the status word)
+            if (ok) {
+                tc_fence_after();
+                for (int i = 0; i < kk; ++i) {
+                    float *part = reinterpret_cast<float *>(gbase) + (i * kRows + r) * p.part_stride;
+                    for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+                        uint32_t v[16];
+                        tmem_ld16(tmem + lane_base + i * p.n_tile + c0, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; e += 4)
+                            *reinterpret_cast<float4 *>(part + c0 + e) =
+                                make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                                            __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+                    }
+                }
+            }
+            fence_proxy_async_smem();   // the staged sums, visible to the bulk copies
+            named_bar_sync(1, 32 * kDequantWarps);
+            if (threadIdx.x == 0) {
+                for (int i = 0; i < kk; ++i)
+                    bulk_s2s_cluster(mapa_shared(base + p.recv_off, static_cast<uint32_t>(i)), base + i * part_bytes,
+                                     part_bytes, mapa_shared(pfull, static_cast<uint32_t>(i)));
+            }
+        } else if (crank < kk) {
+            // head: its own sums (superblocks [0, L)) plus the tail's ([L, nsb)), in that order
+            const int n0 = own_tile * kRows;
+            ok = __all_sync(0xFFFFFFFFu, ok && wait_or_abort(pfull, 0, abort_flag, p.status));
+            const float *part = reinterpret_cast<const float *>(gbase + p.recv_off) + r * p.part_stride;
+            if (ok) {
+                tc_fence_after();
+                for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tmem + lane_base + c0, v);
+                    tmem_wait_ld();
+                    float acc[16];
+#pragma unroll
+                    for (int e = 0; e < 16; e += 4) {
+                        const float4 t4 = *reinterpret_cast<const float4 *>(part + c0 + e);
+                        acc[e] = __uint_as_float(v[e]) + t4.x;
+                        acc[e + 1] = __uint_as_float(v[e + 1]) + t4.y;
+                        acc[e + 2] = __uint_as_float(v[e + 2]) + t4.z;
+                        acc[e + 3] = __uint_as_float(v[e + 3]) + t4.w;
+                    }
+                    if (n0 + r < p.N) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (c0 + i < p.M) p.y[static_cast<int64_t>(c0 + i) * p.N + n0 + r] = acc[i];
+                    }
+                }
+            }
+        }
+    } else if (warp == 8) {
+        // ---------------------------------------------------- weight producer
+        const int nstages = (nv + p.S - 1) / p.S;
+        int issued = 0, s = 0;
+        int tile = tile0, sb = sb0;   // of the stage's first superblock
+        uint32_t ph = 0;
+        for (int si = 0; si < nstages; ++si) {
+            if (!wait_or_abort(qempty(s), ph ^ 1u, abort_flag, p.status)) break;
+            fence_proxy_async_smem();
+            const uint32_t st = q_ring + s * p.q_stage_bytes;
+            const int n0 = tile * kRows;
+            if constexpr (TMA) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(qfull(s), p.q_stage_bytes);
+                    tma_load_2d(st, &wmap, sb * (p.bb / 4), n0, qfull(s));
+                }
+            } else {
+                uint32_t my = 0;
+                const uint8_t *src[4];
+                uint32_t dst[4], nb[4];
+                int tail_len = 0;
+                uint32_t tail_dst = 0;
+                const uint8_t *tail_src = nullptr;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int rr = lane + 32 * i, rowi = n0 + rr;
+                    nb[i] = 0;
+                    src[i] = nullptr;
+                    dst[i] = 0;
+                    if (rowi < p.N) {
+                        const int64_t o = (static_cast<int64_t>(rowi) * p.nsb + sb) * p.bb;
+                        const int64_t lo = o & ~int64_t(15);
+                        int64_t hi = (o + static_cast<int64_t>(p.S) * p.bb + 15) & ~int64_t(15);
+                        const int64_t t16 = p.total_bytes & ~int64_t(15);
+                        if (hi > t16) {
+                            hi = t16;
+                            tail_len = static_cast<int>(o + static_cast<int64_t>(p.S) * p.bb - t16);
+                            tail_src = p.W + t16;
+                            tail_dst = st + rr * p.row_pitch + static_cast<uint32_t>(t16 - lo);
+                        }
+                        const int64_t end = o + static_cast<int64_t>(p.S) * p.bb;
+                        if (in_bounds(lo >= 0 && end <= p.total_bytes && (end + 15 - lo) / 16 * 16 <= p.row_pitch,
+                                      p.status)) {
+                            src[i] = p.W + lo;
+                            dst[i] = st + rr * p.row_pitch;
+                            nb[i] = static_cast<uint32_t>(hi - lo);
+                        } else {
+                            tail_len = 0;
+                        }
+                    }
+                    my += nb[i];
+                }
+                if (tail_len > 0) {
+                    uint8_t *gd = gbase + (tail_dst - base);
+                    for (int i = 0; i < tail_len; ++i) gd[i] = __ldg(tail_src + i);
+                }
+                const uint32_t total = __reduce_add_sync(0xFFFFFFFFu, my);
+                __syncwarp();
+                if (lane == 0) mbar_arrive_expect_tx(qfull(s), total);
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (nb[i]) bulk_g2s(dst[i], src[i], nb[i], qfull(s));
+            }
+            issued = si + 1;
+            step(tile, sb, p.S);
+            if (++s == QS) {
+                s = 0;
+                ph ^= 1u;
+            }
+        }
+        if (*abort_flag) {
+            for (int si = max(0, issued - QS); si < issued; ++si) (void)mbar_wait(qfull(si % QS), (si / QS) & 1);
+        }
+    } else if (warp == 9) {
+        // ---------------------------------------------------- activation producer
+        if (lane == 0) {
+            pdl_wait();
+            int issued = 0;
+            const int nx = (nchunks + p.xk - 1) / p.xk;
+            const uint32_t box_bytes = static_cast<uint32_t>(p.n_tile) * 128u;
+            int s = 0;
+            uint32_t ph = 0;
+            int ct = tile0, csb = sb0, cq = 0;   // position and k chunk of the next chunk
+            for (int xs = 0; xs < nx; ++xs) {
+                if (!wait_or_abort(bempty(s), ph ^ 1u, abort_flag, p.status)) break;
+                const int nb = min(p.xk, nchunks - xs * p.xk);
+                mbar_arrive_expect_tx(bfull(s), nb * box_bytes);
+                for (int i = 0; i < nb; ++i) {
+                    tma_load_2d(b_ring + s * p.b_stage_bytes + i * box_bytes, &xmap, (4 * csb + cq) * kChunkK, 0, bfull(s));
+                    if (++cq == 4) {
+                        cq = 0;
+                        step(ct, csb, 1);
+                    }
+                }
+                issued = xs + 1;
+                if (++s == BS) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (*abort_flag) {
+                for (int c = max(0, issued - BS); c < issued; ++c) (void)mbar_wait(bfull(c % BS), (c / BS) & 1);
+            }
+        }
+    } else {
+        // ---------------------------------------------------- MMA issuer (warp 10)
+        const uint32_t idesc = idesc_f16_f32(kRows, p.n_tile);
+        bool ok = true;
+        const uint32_t box_bytes = static_cast<uint32_t>(p.n_tile) * 128u;
+        int sa = 0, xi = 0, sbb = 0;
+        uint32_t aph = 0, bph = 0;
+        int vt = 0, first = 0;   // tile of position v among the cluster's tiles (tail), v's index in that tile
+        for (int v = 0; v < nv && ok; ++v) {
+            ok = __all_sync(0xFFFFFFFFu, wait_or_abort(afull(sa), aph, abort_flag, p.status));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t a0 = tmem + p.a_col + sa * kASlotCols;
+            const uint32_t d = tmem + static_cast<uint32_t>(vt * p.n_tile);   // the first superblock of a tile overwrites
+#pragma unroll
+            for (int gg = 0; gg < 4; ++gg) {
+                if (xi == 0) {
+                    ok = __all_sync(0xFFFFFFFFu, wait_or_abort(bfull(sbb), bph, abort_flag, p.status));
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                const uint64_t bd = smem_desc_sw128(b_ring + sbb * p.b_stage_bytes + xi * box_bytes);
+                if (elect_one()) {
+#pragma unroll
+                    for (int kq = 0; kq < 4; ++kq)
+                        tc_mma_ts(d, a0 + 32 * gg + 8 * kq, bd + 2 * kq, idesc, (first | gg | kq) != 0);
+                }
+                __syncwarp();
+                if (++xi == p.xk || 4 * v + gg == nchunks - 1) {
+                    if (elect_one()) tc_commit(bempty(sbb));
+                    __syncwarp();
+                    xi = 0;
+                    if (++sbb == BS) {
+                        sbb = 0;
+                        bph ^= 1u;
+                    }
+                }
+            }
+            if (ok) {
+                if (elect_one()) tc_commit(aempty(sa));
+                __syncwarp();
+            }
+            if (++sa == AS) {
+                sa = 0;
+                aph ^= 1u;
+            }
+            if (++first == p.tail && is_tail) {
+                first = 0;
+                ++vt;
+            }
+        }
+        if (elect_one()) tc_commit(accfull);
+        __syncwarp();
+        if (!ok) (void)mbar_wait(accfull, 0);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();   // the tail's staging area stays until every head has its copy
+    if (warp == 10) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
 // ------------------------------------------------------------------------ host side
 
 namespace {
@@ -600,20 +996,34 @@ int pick_n_tile(int64_t M, int64_t N, int num_sms) {
     return best;
 }
 
+// Superblocks per weight stage for the tensor-copy path, and whether the weights take it: whole
+// rows and stages must be 16-byte multiples (Q6_K's 210-byte blocks take per-row bulk copies).
+int tma_stage(int bb, int64_t K) {
+    const int64_t nsb = K / 256;
+    return (bb % 16 == 0) ? 1 : ((2 * bb) % 16 == 0 && nsb % 2 == 0) ? 2 : 1;
+}
+bool block_tma(int type, int bb, int64_t K) {
+    const int64_t nsb = K / 256;
+    return ((nsb * bb) % 16 == 0) && ((tma_stage(bb, K) * bb) % 16 == 0) && type != 14;
+}
+
 struct GemmPlan {
     int n_tile, qstages, bstages, S, xk, a_slots;
     uint32_t a_col;
     bool tma;
-    uint32_t row_pitch, q_stage_bytes, b_stage_bytes, q_off, bar_off;
+    uint32_t row_pitch, q_stage_bytes, b_stage_bytes, q_off, recv_off, bar_off;
     size_t smem;
+    int k, L, tail;   // work split (k > 0): clusters of k heads and one tail CTA
 };
 
-GemmPlan gemm_plan(int type, int bb, int64_t N, int64_t K, int64_t M, int num_sms) {
+// `reserve`: bytes of shared memory kept between the weight ring and the barriers (a split
+// plan's receive area, at recv_off); `n_tile` > 0 fixes the token tile.
+GemmPlan gemm_plan(int type, int bb, int64_t N, int64_t K, int64_t M, int num_sms, uint32_t reserve = 0, int n_tile = 0) {
     GemmPlan pl{};
-    pl.n_tile = pick_n_tile(M, N, num_sms);
+    pl.n_tile = n_tile > 0 ? n_tile : pick_n_tile(M, N, num_sms);
     const int64_t nsb = K / 256;
-    const int s_tma = (bb % 16 == 0) ? 1 : ((2 * bb) % 16 == 0 && nsb % 2 == 0) ? 2 : 1;
-    pl.tma = ((nsb * bb) % 16 == 0) && ((s_tma * bb) % 16 == 0) && type != 14;
+    const int s_tma = tma_stage(bb, K);
+    pl.tma = block_tma(type, bb, K);
     // activation stages of about 32 KB: 1, 2 or 4 chunks of 64 columns
     pl.xk = pl.n_tile >= 256 ? 1 : pl.n_tile >= 128 ? 2 : 4;
     pl.b_stage_bytes = static_cast<uint32_t>(pl.n_tile) * 128u * pl.xk;
@@ -639,8 +1049,9 @@ GemmPlan gemm_plan(int type, int bb, int64_t N, int64_t K, int64_t M, int num_sm
         for (int bs = 4; bs >= 2; --bs) {
             for (int qs = 8; qs >= 2; --qs) {
                 const size_t q_off = static_cast<size_t>(bs) * pl.b_stage_bytes;
-                const size_t bar_off = (q_off + static_cast<size_t>(qs) * q_stage_bytes + 15) & ~size_t(15);
-                const size_t total = bar_off + 8 * (2 * qs + 2 * bs + 2 * kMaxASlots + 1) + 16;
+                const size_t recv_off = (q_off + static_cast<size_t>(qs) * q_stage_bytes + 15) & ~size_t(15);
+                const size_t bar_off = recv_off + reserve;
+                const size_t total = bar_off + 8 * (2 * qs + 2 * bs + 2 * kMaxASlots + kAccBars) + 16;
                 if (total <= limit) {
                     pl.S = S;
                     pl.row_pitch = pitch;
@@ -648,6 +1059,7 @@ GemmPlan gemm_plan(int type, int bb, int64_t N, int64_t K, int64_t M, int num_sm
                     pl.bstages = bs;
                     pl.qstages = qs;
                     pl.q_off = static_cast<uint32_t>(q_off);
+                    pl.recv_off = static_cast<uint32_t>(recv_off);
                     pl.bar_off = static_cast<uint32_t>(bar_off);
                     pl.smem = total + 1024;   // slack for 1024-byte alignment of the base
                     return pl;
@@ -659,27 +1071,133 @@ GemmPlan gemm_plan(int type, int bb, int64_t N, int64_t K, int64_t M, int num_sm
     return pl;
 }
 
-template <int TYPE, bool TMA>
-cudaError_t launch_t(const CUtensorMap &xmap, const CUtensorMap &wmap, const GemmArgs &a, dim3 grid, size_t smem,
-                     bool pdl, cudaStream_t st) {
-    auto kern = gemm_kernel<TYPE, TMA>;
+// The kernel for (type, tma), its shared-memory limit raised once per device.
+template <int TYPE, bool TMA, bool SPLIT>
+const void *kernel_t() {
+    const void *f = SPLIT ? reinterpret_cast<const void *>(gemm_split_kernel<TYPE, TMA>)
+                          : reinterpret_cast<const void *>(gemm_kernel<TYPE, TMA>);
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (e != cudaSuccess) return e;
+        if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
+            return nullptr;
         attr_set[dev] = true;
     }
-    void *args[] = {const_cast<CUtensorMap *>(&xmap), const_cast<CUtensorMap *>(&wmap), const_cast<GemmArgs *>(&a)};
-    return launch_pdl(reinterpret_cast<const void *>(kern), grid, dim3(kThreads), smem, st, pdl, args);
+    return f;
 }
 
 template <int TYPE>
-cudaError_t launch_type(bool tma, const CUtensorMap &xmap, const CUtensorMap &wmap, const GemmArgs &a, dim3 grid,
-                        size_t smem, bool pdl, cudaStream_t st) {
-    return tma ? launch_t<TYPE, true>(xmap, wmap, a, grid, smem, pdl, st)
-               : launch_t<TYPE, false>(xmap, wmap, a, grid, smem, pdl, st);
+const void *kernel_type(bool tma, bool split) {
+    return tma ? (split ? kernel_t<TYPE, true, true>() : kernel_t<TYPE, true, false>())
+               : (split ? kernel_t<TYPE, false, true>() : kernel_t<TYPE, false, false>());
+}
+
+const void *kernel_of(int type, bool tma, bool split) {
+    switch (type) {
+    case 12: return kernel_type<12>(tma, split);
+    case 13: return kernel_type<13>(tma, split);
+    case 14: return kernel_type<14>(tma, split);
+    case kQ6KAligned: return kernel_type<kQ6KAligned>(tma, split);
+    case 23: return kernel_type<23>(tma, split);
+    default: return nullptr;
+    }
+}
+
+// How many clusters of `csize` CTAs of this kernel can be resident at once (clusters are
+// placed within one GPC, so this can be below SMs / csize); cached per device and size.
+int cluster_capacity(const void *f, int csize, size_t smem) {
+    struct Entry {
+        int dev;
+        const void *f;
+        int csize;
+        size_t smem;
+        int n;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    {
+        std::lock_guard<std::mutex> g(mu);
+        for (const Entry &e : cache)
+            if (e.dev == dev && e.f == f && e.csize == csize && e.smem == smem) return e.n;
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(csize));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(csize);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, f, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;   // no split
+    }
+    std::lock_guard<std::mutex> g(mu);
+    cache.push_back({dev, f, csize, smem, n});
+    return n;
+}
+
+// Work split for one token tile whose T row tiles leave SMs idle: clusters of k heads and one
+// tail; a head takes superblocks [0, L) of its row tile and the tail the remaining
+// tail = nsb - L of all k tiles (k divides T), so a CTA's share is max(L, k tail) superblocks against nsb
+// unsplit. Both L and tail are multiples of the weight stage S (no stage spans two tiles); the
+// tail's k accumulators fit below the A ring and its hand-off area below the barriers. Taken
+// when it saves more than one superblock per CTA (the hand-off costs about that).
+template <class Cap>
+void pick_split(GemmPlan &pl, int64_t M, int64_t N, int64_t nsb, int num_sms, Cap cap) {
+    pl.k = 0;
+    const int64_t T = (N + kRows - 1) / kRows;
+    if (M > pl.n_tile || T >= num_sms) return;
+    int64_t best = nsb - 1;
+    for (int k = 1; k <= kMaxSplitK; ++k) {
+        const uint32_t acc_cols = static_cast<uint32_t>(k * pl.n_tile);
+        const uint32_t a_col = std::max<uint32_t>(pl.a_col, (acc_cols + kASlotCols - 1) / kASlotCols * kASlotCols);
+        if (a_col + 2 * kASlotCols > kTmemCols) break;
+        if (static_cast<size_t>(k) * kRows * (pl.n_tile + 4) * 4 > pl.recv_off) break;   // the tail's staging area
+        const int64_t clusters = T / k;   // whole clusters only (every head has a tile)
+        if (T % k != 0 || clusters * (k + 1) > num_sms) continue;
+        for (int64_t tail = pl.S; tail < nsb; tail += pl.S) {
+            const int64_t L = nsb - tail, cost = std::max<int64_t>(L, k * tail);
+            if (cost < best && clusters <= cap(k + 1)) {
+                best = cost;
+                pl.k = k;
+                pl.L = static_cast<int>(L);
+                pl.tail = static_cast<int>(tail);
+            }
+        }
+    }
+    if (pl.k > 0) {
+        pl.a_col = std::max<uint32_t>(pl.a_col, (static_cast<uint32_t>(pl.k * pl.n_tile) + kASlotCols - 1) / kASlotCols *
+                                                    kASlotCols);
+        pl.a_slots = static_cast<int>(std::min<uint32_t>((kTmemCols - pl.a_col) / kASlotCols, kMaxASlots));
+    }
+}
+
+// The launch plan: the unsplit plan, or, for M <= 256, the split form with all M tokens in one
+// tile (a multiple of 16, at least 32) and a row tile's superblocks shared by a cluster, where
+// every CTA keeps a receive area for one tile's partial sums. The split form is taken when its
+// estimate beats the unsplit one, whose token tiles each decode every weight again (costs as in
+// pick_n_tile, plus one superblock for the hand-off). `cap(csize, smem)`: resident clusters.
+template <class Cap>
+GemmPlan choose_plan(int type, int bb, int64_t N, int64_t K, int64_t M, int sms, Cap cap) {
+    GemmPlan pl = gemm_plan(type, bb, N, K, M, sms);
+    if (pl.n_tile == 0 || M > 256) return pl;
+    const int n1 = static_cast<int>(std::max<int64_t>(32, (M + 15) / 16 * 16));
+    GemmPlan ps = gemm_plan(type, bb, N, K, M, sms, static_cast<uint32_t>(kRows * (n1 + 4) * 4), n1);
+    if (ps.n_tile != n1) return pl;
+    pick_split(ps, M, N, K / 256, sms, [&](int csize) { return cap(csize, ps.smem); });
+    const int64_t T = (N + kRows - 1) / kRows, ntok = (M + pl.n_tile - 1) / pl.n_tile;
+    const int64_t cost_plain = (T * ntok + sms - 1) / sms * (K / 256) * std::max<int64_t>(8 * pl.n_tile, 1200);
+    const int64_t cost_split = (std::max<int64_t>(ps.L, static_cast<int64_t>(ps.k) * ps.tail) + 1) *
+                               std::max<int64_t>(8 * n1, 1200);
+    return ps.k > 0 && cost_split < cost_plain ? ps : pl;
 }
 
 }  // namespace
@@ -690,8 +1208,15 @@ cudaError_t gemm_launch(int type, const uint8_t *W, const __half *x, float *y, i
                         unsigned *status, int num_sms, bool pdl, cudaStream_t stream) {
     const int bb = block_bytes_of(type);
     if (bb < 0) return cudaErrorInvalidValue;
-    const GemmPlan pl = gemm_plan(type, bb, N, K, M, num_sms > 0 ? num_sms : 148);
+    const int sms = num_sms > 0 ? num_sms : 148;
+    const void *kern_split = kernel_of(type, block_tma(type, bb, K), true);
+    if (kern_split == nullptr) return cudaErrorInvalidValue;
+    const GemmPlan pl = choose_plan(type, bb, N, K, M, sms, [&](int csize, size_t smem) {
+        return cluster_capacity(kern_split, csize, smem);
+    });
     if (pl.n_tile == 0) return cudaErrorNotSupported;
+    const void *kern = pl.k > 0 ? kern_split : kernel_of(type, pl.tma, false);
+    if (kern == nullptr) return cudaErrorInvalidValue;
     CUtensorMap xmap{}, wmap{};
     if (!encode_tmap_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
                         static_cast<uint64_t>(K) * 2, kChunkK, static_cast<uint32_t>(pl.n_tile), true))
@@ -726,15 +1251,16 @@ cudaError_t gemm_launch(int type, const uint8_t *W, const __half *x, float *y, i
     a.total_bytes = N * (K / 256) * bb;
     a.bb = bb;
     a.type = type;
-    const dim3 grid(static_cast<unsigned>((N + kRows - 1) / kRows), static_cast<unsigned>((M + pl.n_tile - 1) / pl.n_tile));
-    switch (type) {
-    case 12: return launch_type<12>(pl.tma, xmap, wmap, a, grid, pl.smem, pdl, stream);
-    case 13: return launch_type<13>(pl.tma, xmap, wmap, a, grid, pl.smem, pdl, stream);
-    case 14: return launch_type<14>(pl.tma, xmap, wmap, a, grid, pl.smem, pdl, stream);
-    case kQ6KAligned: return launch_type<kQ6KAligned>(pl.tma, xmap, wmap, a, grid, pl.smem, pdl, stream);
-    case 23: return launch_type<23>(pl.tma, xmap, wmap, a, grid, pl.smem, pdl, stream);
-    default: return cudaErrorInvalidValue;
-    }
+    a.row_tiles = static_cast<int>((N + kRows - 1) / kRows);
+    a.k = pl.k;
+    a.L = pl.L;
+    a.tail = pl.tail;
+    a.part_stride = pl.n_tile + 4;
+    a.recv_off = pl.recv_off;
+    const dim3 grid = pl.k > 0 ? dim3(static_cast<unsigned>((a.row_tiles + pl.k - 1) / pl.k * (pl.k + 1)))
+                               : dim3(static_cast<unsigned>(a.row_tiles), static_cast<unsigned>((M + pl.n_tile - 1) / pl.n_tile));
+    void *args[] = {&xmap, &wmap, &a};
+    return launch_pdl(kern, grid, dim3(kThreads), pl.smem, stream, pdl, args, pl.k > 0 ? static_cast<unsigned>(pl.k + 1) : 1u);
 }
 
 }  // namespace ql

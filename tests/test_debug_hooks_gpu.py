@@ -61,6 +61,8 @@ DEBUG_CASES = [
     ("silu", 12, 96, 1024, 1),         # persistent decode kernel, fused prologue
     ("qlinear", 12, 256, 2048, 100),   # tcgen05 prefill GEMM
     ("qlinear", 14, 200, 768, 64),     # prefill GEMM, per-row bulk copies
+    ("qlinear", 12, 640, 4096, 32),    # prefill GEMM, superblocks split over a cluster
+    ("qlinear", 14, 300, 5120, 9),     # split GEMM, per-row bulk copies
 ]
 
 DEBUG_CHILD = r'''

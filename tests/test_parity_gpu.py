@@ -59,7 +59,11 @@ def test_gemv_matches_oracle(ql, t, N, K, M):
 
 
 GEMM_SHAPES = [(128, 256, 32), (129, 512, 9), (300, 1024, 33), (1, 256, 1), (256, 2048, 100), (200, 768, 256),
-               (130, 1280, 300), (128, 512, 512)]
+               (130, 1280, 300), (128, 512, 512),
+               # one token tile over few row tiles: the superblocks of each row tile are split
+               # between a head CTA and a tail CTA of a cluster (ragged rows and tokens), also
+               # where the split plan replaces several token tiles (M = 64, 100, 128)
+               (300, 5120, 9), (640, 4096, 32), (10240, 2048, 16), (1000, 4096, 128), (512, 2048, 64)]
 
 
 @pytest.mark.parametrize("t", TYPES)

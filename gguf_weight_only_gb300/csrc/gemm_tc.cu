@@ -273,6 +273,39 @@ __device__ __forceinline__ void dequant_superblock(uint32_t blk, const KqRow &kr
     }
 }
 
+// ------------------------------------------------------------ clusters (split kernel)
+
+// Barrier `id` (1..15) over `count` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// ---- thread-block clusters and distributed shared memory
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// The shared::cluster address of `addr` (a shared::cta address) in the CTA of rank `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from this CTA's shared
+// memory to another CTA's of the cluster (`dst`, `bar`: shared::cluster addresses); completes
+// as transaction bytes on the destination CTA's mbarrier. The source must have been written
+// before a fence.proxy.async.
+__device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "r"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+// Every thread of every CTA of the cluster: no CTA leaves before all have arrived, so no
+// shared memory another CTA may still read is released early.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ------------------------------------------------------------ bounded waits with abort
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
@@ -1253,7 +1286,22 @@ cudaError_t gemm_launch(int type, const uint8_t *W, const __half *x, float *y, i
     const dim3 grid = pl.k > 0 ? dim3(static_cast<unsigned>((a.row_tiles + pl.k - 1) / pl.k * (pl.k + 1)))
                                : dim3(static_cast<unsigned>(a.row_tiles), static_cast<unsigned>((M + pl.n_tile - 1) / pl.n_tile));
     void *args[] = {&xmap, &wmap, &a};
-    return launch_pdl(kern, grid, dim3(kThreads), pl.smem, stream, pdl, args, pl.k > 0 ? static_cast<unsigned>(pl.k + 1) : 1u);
+    if (pl.k == 0) return launch_pdl(kern, grid, dim3(kThreads), pl.smem, stream, pdl, args);
+    cudaLaunchConfig_t cfg{};   // clusters of k + 1 CTAs along x
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(pl.k + 1);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    return cudaLaunchKernelExC(&cfg, kern, args);
 }
 
 }  // namespace ql

@@ -100,8 +100,6 @@ bool encode_tmap_3d(void *tmap_out, int dtype, const void *base, uint64_t dim0, 
                     bool swizzle128);
 
 // Launch `func` with its argument pointers, optionally as a programmatic dependent launch.
-// cluster > 1: thread-block clusters of `cluster` CTAs along x (grid.x a multiple of it).
-cudaError_t launch_pdl(const void *func, dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl, void **args,
-                       unsigned cluster = 1);
+cudaError_t launch_pdl(const void *func, dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl, void **args);
 
 }  // namespace ql

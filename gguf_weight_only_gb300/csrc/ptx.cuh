@@ -145,36 +145,6 @@ __device__ __forceinline__ bool elect_one() {
         : "=r"(p));
     return p != 0u;
 }
-// Barrier `id` (1..15) over `count` threads (a multiple of 32) of the CTA.
-__device__ __forceinline__ void named_bar_sync(int id, int count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-// ---- thread-block clusters and distributed shared memory
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-// The shared::cluster address of `addr` (a shared::cta address) in the CTA of rank `rank`.
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
-// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from this CTA's shared
-// memory to another CTA's of the cluster (`dst`, `bar`: shared::cluster addresses); completes
-// as transaction bytes on the destination CTA's mbarrier. The source must have been written
-// before a fence.proxy.async.
-__device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "r"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-// Every thread of every CTA of the cluster: no CTA leaves before all have arrived, so no
-// shared memory another CTA may still read is released early.
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 // Block until the preceding kernel in the stream has completed and its writes are visible.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

@@ -559,7 +559,8 @@ TABLE_SHAPES = [
     (12, 4096, 4096, 4), (12, 4096, 12288, 4), (12, 12288, 4096, 4),
     (23, 5120, 5120, 1), (23, 5120, 17408, 1), (23, 17408, 5120, 1),
     (13, 5120, 17408, 1), (14, 5120, 17408, 1),
-    (12, 4096, 12288, 32), (12, 4096, 12288, 128), (12, 4096, 12288, 512),
+    (12, 4096, 12288, 32), (12, 4096, 12288, 64), (12, 4096, 12288, 128), (12, 4096, 12288, 512),
+    (23, 4096, 12288, 32), (12, 4096, 4096, 64), (12, 12288, 4096, 32), (12, 12288, 4096, 128),
     (13, 5120, 17408, 256), (14, 5120, 17408, 256),
     (Q6_K_A16, 5120, 17408, 1), (Q6_K_A16, 5120, 17408, 256),
 ]

@@ -52,10 +52,11 @@ constexpr int kDequantWarps = 8;
 constexpr int kThreads = 32 * 11;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kAccBars = 2;         // accumulator final; (head) the tail's partial sums handed over
-// Heads per tail in the split kernel. Measured on GB300 (M=32, K=4096, N=12288, where pairs
-// would need 192 CTAs): three heads per tail gave Q4_K 18.8 -> 19.4 us, Q5_K 20.6 -> 20.1,
-// Q6_K 39.9 -> 38.3, IQ4_XS 25.9 -> 22.1; pairs gain 1.75-1.9x wherever they fit.
-constexpr int kMaxSplitK = 1;
+// Heads per tail in the split kernel. Measured on GB300 at M=32, K=4096: two heads per tail
+// (where pairs do not fit) gave N=10240 14.8 -> 13.9 us; three gave N=12288 15.0 -> 16.4 us for
+// Q4_K (Q6_K 38.9 -> 37.6, IQ4_XS 21.8 -> 21.3), the tail's serial drain of three tiles costing
+// more than the superblocks saved. Pairs gain 1.75-2.3x wherever they fit.
+constexpr int kMaxSplitK = 2;
 
 struct GemmArgs {
     const uint8_t *W;

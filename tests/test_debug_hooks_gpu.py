@@ -63,6 +63,7 @@ DEBUG_CASES = [
     ("qlinear", 14, 200, 768, 64),     # prefill GEMM, per-row bulk copies
     ("qlinear", 12, 640, 4096, 32),    # prefill GEMM, superblocks split over a cluster
     ("qlinear", 14, 300, 5120, 9),     # split GEMM, per-row bulk copies
+    ("qlinear", 12, 10240, 2048, 16),  # split GEMM, two heads per tail
 ]
 
 DEBUG_CHILD = r'''

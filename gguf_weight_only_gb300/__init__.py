@@ -27,7 +27,7 @@ STATUS = {0: "QL_OK", -1: "QL_ERR_TYPE", -2: "QL_ERR_SHAPE", -3: "QL_ERR_NULL", 
 EXPORTS = ("qlinear", "qlinear_gemv", "qlinear_gemm", "qlinear_block_bytes", "qlinear_gemv_max_m",
            "qlinear_strerror", "qlinear_last_cuda_error", "qlinear_device_status", "qlinear_launch_count",
            "qlinear_selftest_wait_timeout", "qlinear_multi", "qlinear_max_projections", "qlinear_silu_mul",
-           "qlinear_rmsnorm", "qlinear_argmax", "qlinear_embed", "qlinear_repack")
+           "qlinear_rmsnorm", "qlinear_argmax", "qlinear_embed", "qlinear_repack", "qlinear_copy")
 Q6_K_A16 = 270   # Q6_K in 224-byte aligned blocks (qlinear_repack)
 
 _lib = None
@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
         l.qlinear_embed.restype = ctypes.c_int
         l.qlinear_repack.argtypes = [ctypes.c_int, vp, i64, i64, vp, vp]
         l.qlinear_repack.restype = ctypes.c_int
+        l.qlinear_copy.argtypes = [vp, vp, i64, vp]
+        l.qlinear_copy.restype = ctypes.c_int
         _lib = l
     return _lib
 
@@ -352,6 +354,29 @@ def repack(W, ggml_type: int, N: int, K: int, out=None, stream=None):
         _check(lib().qlinear_repack(int(ggml_type), W.data_ptr(), int(N), int(K), out.data_ptr(),
                                     _stream_handle(stream)), "qlinear_repack")
     return out
+
+
+def copy(dst, src, stream=None):
+    """dst[:] = src (same number of bytes, both contiguous) by the library's copy kernel, for
+    moving a step's inputs in and outputs out around its layer calls. Each tensor is on the one
+    CUDA device involved or in page-locked host memory (`pin_memory()`), which the kernel reads
+    or writes directly. Asynchronous on the device's current stream (or `stream`)."""
+    import torch
+    for name, t in (("dst", dst), ("src", src)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError(f"{name} must be a CUDA tensor or page-locked host memory")
+    nbytes = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != nbytes:
+        raise ValueError(f"dst has {nbytes} bytes, src {src.numel() * src.element_size()}")
+    cuda = [t for t in (dst, src) if t.is_cuda]
+    dev_ctx = _device_of(*cuda) if cuda else torch.cuda.device(torch.cuda.current_device())
+    with dev_ctx:
+        if stream is not None and cuda:
+            _check_stream(stream, cuda[0])
+        _check(lib().qlinear_copy(dst.data_ptr(), src.data_ptr(), int(nbytes), _stream_handle(stream)), "qlinear_copy")
+    return dst
 
 
 def device_status(stream=None) -> int:

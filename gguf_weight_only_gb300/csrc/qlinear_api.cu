@@ -125,6 +125,38 @@ __global__ void status_take_kernel(unsigned *word, unsigned *out) { *out = atomi
 // Does nothing: launched the ordinary way (no programmatic dependent launch) it orders the stream.
 __global__ void stream_fence_kernel() {}
 
+// qlinear_copy's kernel: 16 bytes per thread and step where both ends are 16-byte aligned, else
+// byte by byte. It lets the next kernel launch first and waits for the preceding one before
+// touching either buffer.
+__global__ void copy_kernel(uint8_t *dst, const uint8_t *src, int64_t bytes) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int64_t head = 0;
+    if (((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 15u) == 0) {
+        const int64_t n16 = bytes / 16;
+        for (int64_t i = tid; i < n16; i += nthr)
+            reinterpret_cast<uint4 *>(dst)[i] = reinterpret_cast<const uint4 *>(src)[i];
+        head = n16 * 16;
+    }
+    for (int64_t i = head + tid; i < bytes; i += nthr) dst[i] = src[i];
+}
+
+// The address a kernel uses for `ptr`: itself for device (or managed) memory of the current
+// device, the mapped device address for page-locked host memory; nullptr for anything else.
+void *kernel_address(const DeviceState &s, const void *ptr) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+        (void)cudaGetLastError();   // an unknown pointer: not an error of the context
+        return nullptr;
+    }
+    if ((at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) && at.device == s.dev)
+        return const_cast<void *>(ptr);
+    if (at.type == cudaMemoryTypeHost && at.devicePointer != nullptr) return at.devicePointer;
+    return nullptr;
+}
+
 // One thread waits, with the library's bounded wait, on a barrier phase that never
 // completes; when the wait runs out it records the timeout in the status word.
 __global__ void wait_timeout_selftest_kernel(unsigned *status) {
@@ -266,6 +298,26 @@ int qlinear_repack(int type, const void *W_src, int64_t N, int64_t K, void *W_ds
     // that follows may then start early without seeing W_dst half written.
     stream_fence_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>();
     e = cudaGetLastError();
+    return e == cudaSuccess ? QL_OK : cuda_fail(e);
+}
+
+int qlinear_copy(void *dst, const void *src, int64_t bytes, void *stream) {
+    if (bytes < 0) return QL_ERR_SHAPE;
+    if (bytes == 0) return QL_OK;
+    if (!dst || !src) return QL_ERR_NULL;
+    DeviceState *s = nullptr;
+    int rc = device_state(&s);
+    if (rc != QL_OK) return rc;
+    void *d = kernel_address(*s, dst);
+    const void *sp = kernel_address(*s, src);
+    if (!d || !sp) return QL_ERR_DEVICE;
+    if (launch_refused(*s)) return QL_ERR_CUDA;
+    constexpr int kThreadsCopy = 256;
+    const int64_t units = (bytes + 15) / 16;
+    const int64_t blocks = std::min<int64_t>((units + kThreadsCopy - 1) / kThreadsCopy, int64_t(4) * s->num_sms);
+    void *args[] = {&d, const_cast<void **>(&sp), &bytes};
+    const cudaError_t e = ql::launch_pdl(reinterpret_cast<const void *>(copy_kernel), dim3(static_cast<unsigned>(blocks)),
+                                         dim3(kThreadsCopy), 0, static_cast<cudaStream_t>(stream), s->pdl, args);
     return e == cudaSuccess ? QL_OK : cuda_fail(e);
 }
 

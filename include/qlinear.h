@@ -142,6 +142,22 @@ int qlinear_max_projections(void);
 int qlinear_repack(int type, const void *W_src, int64_t N, int64_t K, void *W_dst, void *stream);
 
 /*
+ * qlinear_copy: copies `bytes` from src to dst on `stream` with a kernel, for moving a layer's
+ * inputs in and its outputs out around the layer calls of a step. Each pointer is device
+ * memory of the current device or page-locked host memory mapped into the device's address
+ * space (cudaHostAlloc / cudaHostRegister memory on a system with unified addressing); a
+ * host pointer is read or written by the kernel directly, with no staging buffer. Anything
+ * else gives QL_ERR_DEVICE before any launch. The regions must not overlap; bytes == 0 does
+ * nothing; bytes < 0 gives QL_ERR_SHAPE; a NULL pointer (bytes > 0) gives QL_ERR_NULL.
+ * The kernel is a programmatic dependent launch like the layer kernels (it lets the next
+ * kernel start at once and waits for the preceding one before touching memory), so a layer
+ * call right after it streams its weights while the copy runs, and a copy right after a
+ * layer call starts as that call drains. Asynchronous; the bytes are in dst once the stream
+ * has reached the copy's end (e.g. after a stream synchronize for a host dst).
+ */
+int qlinear_copy(void *dst, const void *src, int64_t bytes, void *stream);
+
+/*
  * Decode calls with the layer's input produced inside the launch (fused prologue) and an
  * optional residual added to the output (fused epilogue). The pages fuse both element-wise
  * producers into the consuming linear and check the result equals the separate steps

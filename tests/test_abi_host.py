@@ -248,3 +248,21 @@ def test_repack_bad_arguments_rejected_before_launch(lib, case):
     t, src, N, K, dst, expect = case
     v = lambda p: ctypes.c_void_p(p or None)
     assert lib.qlinear_repack(t, v(src), N, K, v(dst), None) == expect
+
+
+# ------------------------------------------------------------------ qlinear_copy
+
+def test_copy_bad_arguments_rejected_before_launch(lib):
+    assert lib.qlinear_copy(ctypes.c_void_p(16), ctypes.c_void_p(16), -1, None) == -2    # bytes < 0
+    assert lib.qlinear_copy(ctypes.c_void_p(None), ctypes.c_void_p(16), 8, None) == -3  # null dst
+    assert lib.qlinear_copy(ctypes.c_void_p(16), ctypes.c_void_p(None), 8, None) == -3  # null src
+    assert lib.qlinear_copy(ctypes.c_void_p(None), ctypes.c_void_p(None), 0, None) == 0  # nothing to do
+
+
+def test_copy_wrapper_checks_its_tensors(lib):
+    import torch
+    a = torch.zeros(8, dtype=torch.float32)
+    with pytest.raises(ValueError):   # plain (pageable) host memory
+        ql.copy(a, torch.zeros(8, dtype=torch.float32))
+    with pytest.raises(ValueError):   # not contiguous
+        ql.copy(torch.zeros(4, 4)[:, 1], torch.zeros(4))

@@ -360,7 +360,9 @@ def copy(dst, src, stream=None):
     """dst[:] = src (same number of bytes, both contiguous) by the library's copy kernel, for
     moving a step's inputs in and outputs out around its layer calls. Each tensor is on the one
     CUDA device involved or in page-locked host memory (`pin_memory()`), which the kernel reads
-    or writes directly. Asynchronous on the device's current stream (or `stream`)."""
+    or writes directly. Asynchronous on the device's current stream (or `stream`). The copy
+    kernel lets the next kernel start at once, so it is not for weights a layer call reads right
+    after it (the layer kernels fetch W before waiting for the kernels ahead of them)."""
     import torch
     for name, t in (("dst", dst), ("src", src)):
         if not t.is_contiguous():

@@ -36,9 +36,10 @@
  * Weights and the preceding kernel: the layer kernels are launched with programmatic dependent
  * launch (unless the environment sets QL_PDL=0) and start fetching W before the kernel ahead of
  * them in the stream has finished; only x (and the other inputs) are read after it completes.
- * So W must not be written by the kernel that immediately precedes the call on its stream.
- * qlinear_repack keeps this by ending with an empty ordinary launch; a caller that writes W
- * with its own kernel right before a call puts any other work (or an event wait) in between,
+ * So W must not be written by the kernel that immediately precedes the call on its stream, nor
+ * by an earlier one linked to the call through kernels that also start early (qlinear_copy is
+ * one). qlinear_repack keeps this by ending with an empty ordinary launch; a caller that writes
+ * W with its own kernel right before a call puts any other work (or an event wait) in between,
  * or sets QL_PDL=0.
  *
  * Errors: arguments are checked on the host before any launch, and a failing check
@@ -152,8 +153,11 @@ int qlinear_repack(int type, const void *W_src, int64_t N, int64_t K, void *W_ds
  * The kernel is a programmatic dependent launch like the layer kernels (it lets the next
  * kernel start at once and waits for the preceding one before touching memory), so a layer
  * call right after it streams its weights while the copy runs, and a copy right after a
- * layer call starts as that call drains. Asynchronous; the bytes are in dst once the stream
- * has reached the copy's end (e.g. after a stream synchronize for a host dst).
+ * layer call starts as that call drains. For the same reason it is for a step's inputs and
+ * outputs, not for a layer's weights: copied W must be separated from the layer calls that read
+ * it by an ordinary launch, an event wait or a synchronisation (see "Weights and the preceding
+ * kernel"). Asynchronous; the bytes are in dst once the stream has reached the copy's end (e.g.
+ * after a stream synchronize for a host dst).
  */
 int qlinear_copy(void *dst, const void *src, int64_t bytes, void *stream);
 

@@ -164,12 +164,15 @@ def test_unit_activation_prefill(ql, t):
 @pytest.mark.parametrize("path", ["gemv", "gemm"])
 @pytest.mark.parametrize("t", TYPES)
 def test_deterministic(ql, path, t):
-    N, K, M = 257, 2048, 6 if path == "gemv" else 48
-    W = synth.weights(t, N, K, [420, t])
-    x = synth.activations(M, K, [421, t])
-    a = run(ql, path, t, W, N, K, x)
-    b = run(ql, path, t, W, N, K, x)
-    assert np.array_equal(a.view(np.uint64), b.view(np.uint64))
+    # gemm: M=48 takes the split form (each row tile's sums from a CTA pair, added in a fixed
+    # order), M=300 one CTA per row tile and token tile
+    for M in ((6,) if path == "gemv" else (48, 300)):
+        N, K = 257, 2048
+        W = synth.weights(t, N, K, [420, t])
+        x = synth.activations(M, K, [421, t])
+        a = run(ql, path, t, W, N, K, x)
+        b = run(ql, path, t, W, N, K, x)
+        assert np.array_equal(a.view(np.uint64), b.view(np.uint64)), M
 
 
 @pytest.mark.parametrize("t", TYPES)

@@ -64,7 +64,8 @@ GEMM_SHAPES = [(128, 256, 32), (129, 512, 9), (300, 1024, 33), (1, 256, 1), (256
                # between a head CTA and a tail CTA of a cluster (ragged rows and tokens), also
                # where the split plan replaces several token tiles (M = 64, 100, 128); 80 row
                # tiles take two heads per tail on 152 SMs
-               (300, 5120, 9), (640, 4096, 32), (10240, 2048, 16), (1000, 4096, 128), (512, 2048, 64)]
+               (300, 5120, 9), (640, 4096, 32), (10240, 2048, 16), (1000, 4096, 128), (512, 2048, 64),
+               (1, 4096, 3)]
 
 
 @pytest.mark.parametrize("t", TYPES)

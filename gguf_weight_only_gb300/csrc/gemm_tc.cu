@@ -823,9 +823,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      part_bytes, mapa_shared(pfull, static_cast<uint32_t>(i)));
             }
         } else if (crank < kk) {
-            // head: its own sums (superblocks [0, L)) plus the tail's ([L, nsb)), in that order
+            // head: its own sums (superblocks [0, L)) plus the tail's ([L, nsb)), in that order.
+            // The tail's copy is waited for even after an abort (the tail sends it regardless), so
+            // that it has landed before this CTA's shared memory is released; the wait is bounded.
             const int n0 = own_tile * kRows;
-            ok = __all_sync(0xFFFFFFFFu, ok && wait_or_abort(pfull, 0, abort_flag, p.status));
+            const bool landed = mbar_wait(pfull, 0);
+            if (!landed && lane == 0) atomicOr(p.status, kStatusTimeout);
+            ok = __all_sync(0xFFFFFFFFu, ok && landed);
             const float *part = reinterpret_cast<const float *>(gbase + p.recv_off) + r * p.part_stride;
             if (ok) {
                 tc_fence_after();

@@ -146,15 +146,17 @@ def test_unit_activation_single_token(ql, t):
 
 
 @pytest.mark.parametrize("t", TYPES)
-def test_unit_activation_prefill(ql, t):
-    """x = e_k through the tcgen05 prefill kernel (M = 40 tokens, token m picks column k_m):
-    its dequantisers form each weight in fp32 and round it once to fp16 for tensor memory, so
-    y is the weight to 11 significant bits (2^-24 absolute below fp16's normal range, where
-    a weight that nearly cancels to zero lands on the subnormal grid)."""
+@pytest.mark.parametrize("M", [40, 300])
+def test_unit_activation_prefill(ql, t, M):
+    """x = e_k through the tcgen05 prefill kernels (token m picks column k_m; M = 40 takes the
+    split form, each row tile's superblocks shared by a CTA pair, M = 300 one CTA per tile): the
+    dequantisers form each weight in fp32 and round it once to fp16 for tensor memory, so y is
+    the weight to 11 significant bits (2^-24 absolute below fp16's normal range, where a weight
+    that nearly cancels to zero lands on the subnormal grid)."""
     N, K = 200, 1024
     W = synth.weights(t, N, K, [412, t])
     w = oracle.dequant(t, W, N, K)
-    ks = [(37 * m) % K for m in range(40)]
+    ks = [(37 * m) % K for m in range(M)]
     x = np.zeros((len(ks), K), np.float16)
     for m, k in enumerate(ks):
         x[m, k] = 1.0

@@ -202,6 +202,9 @@ FULL = [
     (23, 5120, 5120, 1), (23, 5120, 17408, 1), (23, 17408, 5120, 1),
     (12, 4096, 12288, 32), (12, 4096, 12288, 128), (12, 4096, 12288, 512),
     (13, 5120, 17408, 1), (13, 5120, 17408, 256), (14, 5120, 17408, 1), (14, 5120, 17408, 256),
+    # the split prefill form at full size: CTA pairs (K=12288 N=4096, K=17408 N=5120) and two
+    # heads per tail (N=10240, 80 row tiles)
+    (12, 12288, 4096, 32), (12, 12288, 4096, 128), (23, 17408, 5120, 32), (14, 17408, 5120, 32), (13, 4096, 10240, 32),
 ]
 
 

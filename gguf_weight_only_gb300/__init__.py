@@ -27,7 +27,7 @@ STATUS = {0: "QL_OK", -1: "QL_ERR_TYPE", -2: "QL_ERR_SHAPE", -3: "QL_ERR_NULL", 
 EXPORTS = ("qlinear", "qlinear_gemv", "qlinear_gemm", "qlinear_block_bytes", "qlinear_gemv_max_m",
            "qlinear_strerror", "qlinear_last_cuda_error", "qlinear_device_status", "qlinear_launch_count",
            "qlinear_selftest_wait_timeout", "qlinear_multi", "qlinear_max_projections", "qlinear_silu_mul",
-           "qlinear_rmsnorm", "qlinear_argmax", "qlinear_embed", "qlinear_repack", "qlinear_copy")
+           "qlinear_rmsnorm", "qlinear_argmax", "qlinear_embed", "qlinear_repack", "qlinear_copy", "qlinear_gemm_plan")
 Q6_K_A16 = 270   # Q6_K in 224-byte aligned blocks (qlinear_repack)
 
 _lib = None
@@ -82,6 +82,9 @@ def lib() -> ctypes.CDLL:
         l.qlinear_repack.restype = ctypes.c_int
         l.qlinear_copy.argtypes = [vp, vp, i64, vp]
         l.qlinear_copy.restype = ctypes.c_int
+        l.qlinear_gemm_plan.argtypes = [ctypes.c_int, i64, i64, i64, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
+                                        ctypes.POINTER(i64)]
+        l.qlinear_gemm_plan.restype = ctypes.c_int
         _lib = l
     return _lib
 
@@ -379,6 +382,22 @@ def copy(dst, src, stream=None):
             _check_stream(stream, cuda[0])
         _check(lib().qlinear_copy(dst.data_ptr(), src.data_ptr(), int(nbytes), _stream_handle(stream)), "qlinear_copy")
     return dst
+
+
+GEMM_PLAN_FIELDS = ("n_tile", "k", "L", "tail", "S", "xk", "a_col", "a_slots", "recv_off", "bar_off", "grid_x",
+                    "grid_y", "cluster", "smem")
+
+
+def gemm_plan(ggml_type: int, N: int, K: int, M: int, num_sms: int, cluster_capacity=None) -> dict:
+    """The prefill GEMM's launch plan for this shape, computed on the host (no device needed):
+    num_sms SMs and cluster_capacity[i] resident clusters of i + 2 CTAs (None: no clusters)."""
+    caps = None
+    if cluster_capacity is not None:
+        vals = list(cluster_capacity)[:7] + [0] * (7 - len(list(cluster_capacity)[:7]))
+        caps = (ctypes.c_int * 7)(*vals)
+    out = (ctypes.c_int64 * 14)()
+    _check(lib().qlinear_gemm_plan(int(ggml_type), int(N), int(K), int(M), int(num_sms), caps, out), "qlinear_gemm_plan")
+    return dict(zip(GEMM_PLAN_FIELDS, (int(v) for v in out)))
 
 
 def device_status(stream=None) -> int:

@@ -1235,6 +1235,37 @@ GemmPlan choose_plan(int type, int bb, int64_t N, int64_t K, int64_t M, int sms,
 
 int gemm_launch_count(int, int64_t, int64_t, int64_t) { return 1; }
 
+// The plan gemm_launch makes, without a device: num_sms SMs and caps[i] resident clusters of
+// i + 2 CTAs (i = 0..6; null: none). out[14] = {n_tile, k, L, tail, S, xk, a_col, a_slots,
+// recv_off, bar_off, grid_x, grid_y, cluster size, dynamic shared memory bytes}; k = 0 is the
+// unsplit kernel (one CTA per row tile and token tile). 0, or -1 for an unknown type, -7 when
+// no plan fits.
+int gemm_plan_info(int type, int64_t N, int64_t K, int64_t M, int num_sms, const int *caps, int64_t *out) {
+    const int bb = block_bytes_of(type);
+    if (bb < 0) return -1;
+    const GemmPlan pl = choose_plan(type, bb, N, K, M, num_sms, [&](int csize, size_t) {
+        return caps != nullptr && csize >= 2 && csize <= 8 ? caps[csize - 2] : 0;
+    });
+    if (pl.n_tile == 0) return -7;
+    const int64_t T = (N + kRows - 1) / kRows;
+    const int64_t v[14] = {pl.n_tile,
+                           pl.k,
+                           pl.L,
+                           pl.tail,
+                           pl.S,
+                           pl.xk,
+                           pl.a_col,
+                           pl.a_slots,
+                           pl.recv_off,
+                           pl.bar_off,
+                           pl.k > 0 ? (T + pl.k - 1) / pl.k * (pl.k + 1) : T,
+                           pl.k > 0 ? 1 : (M + pl.n_tile - 1) / pl.n_tile,
+                           pl.k > 0 ? pl.k + 1 : 1,
+                           static_cast<int64_t>(pl.smem)};
+    for (int i = 0; i < 14; ++i) out[i] = v[i];
+    return 0;
+}
+
 cudaError_t gemm_launch(int type, const uint8_t *W, const __half *x, float *y, int64_t N, int64_t K, int64_t M,
                         unsigned *status, int num_sms, bool pdl, cudaStream_t stream) {
     const int bb = block_bytes_of(type);

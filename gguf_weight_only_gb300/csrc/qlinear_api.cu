@@ -9,6 +9,11 @@
 #include "ptx.cuh"
 #include "qlinear.h"
 
+namespace ql {
+// gemm_tc.cu: the prefill plan without a device (see qlinear_gemm_plan)
+int gemm_plan_info(int type, int64_t N, int64_t K, int64_t M, int num_sms, const int *caps, int64_t *out);
+}  // namespace ql
+
 namespace {
 
 // Device status word: kernels OR error bits into it (a bounded wait that ran out, an embedding
@@ -433,6 +438,17 @@ int qlinear_device_status(void *stream) {
     if (word & ql::kStatusBounds) return QL_ERR_BOUNDS;
     if (word & ql::kStatusTimeout) return QL_ERR_TIMEOUT;
     return word ? QL_ERR_INDEX : QL_OK;
+}
+
+int qlinear_gemm_plan(int type, int64_t N, int64_t K, int64_t M, int num_sms, const int *cluster_capacity,
+                      int64_t *plan) {
+    if (ql::block_bytes_of(type) < 0) return QL_ERR_TYPE;
+    if (N < 1 || M < 1 || K < 256 || K % 256 != 0 || N > (int64_t(1) << 30) || K > (int64_t(1) << 24) ||
+        M > kMaxTokens || num_sms < 1)
+        return QL_ERR_SHAPE;
+    if (!plan) return QL_ERR_NULL;
+    const int rc = ql::gemm_plan_info(type, N, K, M, num_sms, cluster_capacity, plan);
+    return rc == 0 ? QL_OK : rc == -1 ? QL_ERR_TYPE : QL_ERR_UNSUPPORTED;
 }
 
 int qlinear_launch_count(int type, int64_t N, int64_t K, int64_t M) {

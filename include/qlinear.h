@@ -239,6 +239,25 @@ int qlinear_device_status(void *stream);
  * QL_ERR_* on invalid arguments. */
 int qlinear_launch_count(int type, int64_t N, int64_t K, int64_t M);
 
+/*
+ * qlinear_gemm_plan: the launch plan of the prefill GEMM (M > 8) for this shape, computed on
+ * the host without a device, for tests and tooling. num_sms: the device's SM count;
+ * cluster_capacity[i]: how many thread-block clusters of i + 2 CTAs can be resident at once
+ * (i = 0..6; NULL: none, so no split plan). plan[14] receives {n_tile, k, L, tail, S, xk,
+ * a_col, a_slots, recv_off, bar_off, grid_x, grid_y, cluster, smem}:
+ *   n_tile  tokens per tile;  k  heads per tail CTA (0: one CTA per row tile and token tile);
+ *   L, tail superblocks [0, L) of a row tile go to its head, [L, K/256) to the tail;
+ *   S       superblocks per weight stage;  xk  64-wide k chunks per x stage;
+ *   a_col, a_slots  first TMEM column and depth (superblocks) of the dequantised-weight ring;
+ *   recv_off, bar_off  shared-memory offsets of the split form's receive area and barriers;
+ *   grid_x, grid_y, cluster, smem  the launch (cluster: CTAs per cluster, 1 = none).
+ * The device call makes the same plan with the device's SM count and cudaOccupancyMaxActiveClusters.
+ * QL_ERR_TYPE, QL_ERR_SHAPE (as qlinear, or num_sms < 1), QL_ERR_NULL (plan), or
+ * QL_ERR_UNSUPPORTED when no plan fits in shared memory.
+ */
+int qlinear_gemm_plan(int type, int64_t N, int64_t K, int64_t M, int num_sms, const int *cluster_capacity,
+                      int64_t *plan);
+
 /* Diagnostic of the failure path: enqueues on `stream` one small kernel whose bounded wait
  * on a barrier that nothing completes runs out (after about 2 s) and sets the device status
  * word, exactly as an expired pipeline wait in the layer's kernels would. No fault is raised
